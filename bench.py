@@ -1,0 +1,480 @@
+"""Benchmark: DCP-sharded decode attention + LSE merge on one GB300.
+
+One step = dcp_decode_attn (all shards) + dcp_merge over one decode batch of
+the named workload (default: MLA, batch 512, Lq 1, dcp_size 8, interleave 128,
+log-normal context lengths with median 67k; about 40 GB of bf16 latent cache).
+The cache is resident in HBM; it is larger than L2, so no flush is needed
+between steps.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Metric: KV-cache GB/s (algorithmic cache bytes of the step / step time), with
+the step's fraction of its HBM/tensor roofline and query-tokens/s alongside.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from context_decode_attention_paged_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "KV GB/s & % roofline, DCP-sharded MLA/GQA decode attn + LSE merge, 1xGB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------
+# roofline arithmetic (per unit of work)
+# ---------------------------------------------------------------------------
+
+def kv_bytes_per_token(w: wl.Workload) -> int:
+    """Cache bytes one token contributes (MLA: the value is a prefix of the key row)."""
+    if w.kind == "mla":
+        return w.head_dim_qk * 2
+    return w.num_kv_heads * (w.head_dim_qk + w.head_dim_v) * 2
+
+
+def visible_keys(w: wl.Workload, seq_lens) -> int:
+    """Sum over (b, i) of keys query i sees (S - Lq + i + 1)."""
+    s = np.asarray(seq_lens, dtype=np.int64)
+    return int(sum((s - w.q_len + i + 1).sum() for i in range(w.q_len)))
+
+
+def algorithmic(w: wl.Workload, seq_lens) -> dict:
+    B, Lq, Hq, N = w.batch, w.q_len, w.num_q_heads, w.dcp_size
+    tokens = int(np.asarray(seq_lens, dtype=np.int64).sum())
+    kv = tokens * kv_bytes_per_token(w)
+    q = B * Lq * Hq * w.head_dim_qk * 2
+    partials = N * B * Lq * Hq * (w.head_dim_v + 1) * 4          # written once, read once
+    out = B * Lq * Hq * w.head_dim_v * 2 + B * Lq * Hq * 4
+    flops = 2 * (w.head_dim_qk + w.head_dim_v) * Hq * visible_keys(w, seq_lens)
+    return {"kv_bytes": kv, "tokens": tokens,
+            "attn_bytes": kv + q + partials,                       # the attention kernel
+            "merge_bytes": partials + out,
+            "step_bytes": kv + q + 2 * partials + out,
+            "flops": flops}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workload set-up (GPU leg): block counts come from the library's slot map
+# ---------------------------------------------------------------------------
+
+def setup_gpu(w: wl.Workload, rank: int):
+    from context_decode_attention_paged_gb300 import binding as dcp
+    seq_lens = wl.make_seq_lens(w)
+    sl_dev = seq_lens.cuda()
+    _, lnb, _, _ = dcp.dcp_build_slot_map(sl_dev, w.block_size, w.interleave, w.dcp_size)
+    torch.cuda.synchronize()
+    inst = wl.make_instance(w, lnb.cpu(), device="cuda", seq_lens=seq_lens)
+    return inst
+
+
+def step_fn(inst, po, lse, out, out_lse, ws):
+    from context_decode_attention_paged_gb300 import binding as dcp
+    w = inst.w
+
+    def attn():
+        dcp.dcp_decode_attn(w.kind, inst.q, inst.kv_cache, inst.block_tables, inst.seq_lens,
+                            w.dcp_size, w.interleave, w.scale, w.q_len, w.head_dim_v,
+                            partial_out=po, lse=lse, workspace=ws)
+
+    def merge():
+        dcp.dcp_merge(po, lse, w.dcp_size, out=out, out_lse=out_lse)
+
+    return attn, merge
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as td
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if td.get_backend() == "nccl" else "cpu")
+    td.all_reduce(t, op=td.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as td
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if td.get_backend() == "nccl" else "cpu")
+    td.all_reduce(t, op=td.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as td
+        td.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+def host_sample(inst, idx):
+    """q, a compact host copy of the blocks the sampled requests use, remapped
+    block tables and lengths for the requests ``idx``."""
+    w = inst.w
+    bt = inst.block_tables.cpu()[:, idx]                     # [N][b][max_lb]
+    sl = inst.seq_lens.cpu()[idx]
+    from oracle import dcp_oracle as orc
+    used, tables = [], torch.zeros_like(bt)
+    for r in range(w.dcp_size):
+        for k, b in enumerate(idx):
+            n_local = len(orc.shard_token_lists(int(sl[k]), w.interleave, w.dcp_size)[r])
+            nb = -(-n_local // w.block_size)
+            ids = bt[r, k, :nb]
+            tables[r, k, :nb] = torch.arange(len(used), len(used) + nb, dtype=torch.int32)
+            used.extend(ids.tolist())
+    ids = torch.tensor(used, dtype=torch.int64, device=inst.kv_cache.device)
+    if w.kind == "gqa":
+        kv = inst.kv_cache[:, ids].cpu()
+    else:
+        kv = inst.kv_cache[ids].cpu()
+    q = inst.q[torch.as_tensor(idx, device=inst.q.device)].cpu()
+    return q, kv, tables.numpy(), sl.numpy()
+
+
+def oracle_time(inst, budget_s: float, max_seqs: int):
+    """Run the oracle over requests 0, 1, ... until ``budget_s`` of CPU time;
+    returns (seconds, cache bytes covered, requests, query tokens)."""
+    from oracle import dcp_oracle as orc
+    w = inst.w
+    done, secs, kv_bytes, qtok = 0, 0.0, 0, 0
+    while done < min(max_seqs, w.batch) and (secs < budget_s or done < 1):
+        q, kv, bt, sl = host_sample(inst, [done])
+        q64, kv64 = orc.to_f64(q), orc.to_f64(kv)
+        t0 = time.perf_counter()
+        orc.ref_dcp_decode(w.kind, q64, kv64, bt, sl, w.dcp_size, w.interleave, w.block_size,
+                           w.scale, w.q_len, w.head_dim_v)
+        secs += time.perf_counter() - t0
+        kv_bytes += int(sl.sum()) * kv_bytes_per_token(w)
+        qtok += w.q_len
+        done += 1
+    return secs, kv_bytes, done, qtok
+
+
+def cpu_threads() -> int:
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        n = [i.get("num_threads") for i in info if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# main legs
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as td
+        td.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from context_decode_attention_paged_gb300 import binding as dcp
+    w = wl.WORKLOADS[args.workload].with_(seed=wl.WORKLOADS[args.workload].seed + rank)
+    inst = setup_gpu(w, rank)
+    N, B, Lq, Hq, Dv = w.dcp_size, w.batch, w.q_len, w.num_q_heads, w.head_dim_v
+    dev = torch.device("cuda", local)
+    po = torch.empty((N, B, Lq, Hq, Dv), dtype=torch.float32, device=dev)
+    lse = torch.empty((N, B, Lq, Hq), dtype=torch.float32, device=dev)
+    out = torch.empty((N, B, Lq, Hq // N, Dv), dtype=torch.bfloat16, device=dev)
+    out_lse = torch.empty((N, B, Lq, Hq // N), dtype=torch.float32, device=dev)
+    desc = dcp.desc_from_tensors(w.kind, inst.q, inst.kv_cache, inst.block_tables, Dv)
+    ws_bytes = dcp.dcp_decode_attn_workspace_size(desc, N)
+    ws = torch.empty((max(ws_bytes, 1),), dtype=torch.uint8, device=dev) if ws_bytes else None
+    attn, merge = step_fn(inst, po, lse, out, out_lse, ws)
+    launches_per_step = (2 if ws_bytes else 1) + 1
+    alg = algorithmic(w, inst.seq_lens.cpu().numpy())
+
+    for _ in range(args.warmup):
+        attn()
+        merge()
+    torch.cuda.synchronize()
+    st = dcp.dcp_get_last_device_status()
+    if st != dcp.DCP_OK:
+        raise RuntimeError(f"device status after warm-up: {dcp.status_string(st)}")
+
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps + 1)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        ev[0].record(stream)
+        for k in range(args.steps):
+            attn()
+            ev[2 * k + 1].record(stream)
+            merge()
+            ev[2 * k + 2].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = ev[0].elapsed_time(ev[-1])
+    attn_ms = [ev[2 * k].elapsed_time(ev[2 * k + 1]) for k in range(args.steps)]
+    merge_ms = [ev[2 * k + 1].elapsed_time(ev[2 * k + 2]) for k in range(args.steps)]
+    st = dcp.dcp_get_last_device_status()
+    if st != dcp.DCP_OK:
+        raise RuntimeError(f"device status after timing: {dcp.status_string(st)}")
+
+    # e2e through the same calls with host buffers: q, block tables and lengths
+    # are copied in from pinned memory and the merged output read back each step
+    q_h = inst.q.cpu().pin_memory()
+    bt_h = inst.block_tables.cpu().pin_memory()
+    sl_h = inst.seq_lens.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(out_lse.shape, dtype=out_lse.dtype).pin_memory()
+    e2e_steps = max(3, min(args.steps, 10))
+    for k in range(2):
+        inst.q.copy_(q_h, non_blocking=True)
+        attn()
+        merge()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    t0.record(stream)
+    for k in range(e2e_steps):
+        inst.q.copy_(q_h, non_blocking=True)
+        inst.block_tables.copy_(bt_h, non_blocking=True)
+        inst.seq_lens.copy_(sl_h, non_blocking=True)
+        attn()
+        merge()
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(out_lse, non_blocking=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = t0.elapsed_time(t1) / e2e_steps
+    h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+    ms_per_step = max_over_ranks(total_ms / args.steps, world)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    kv_all = sum_over_ranks(float(alg["kv_bytes"]), world)
+    qtok_all = sum_over_ranks(float(B * Lq), world)
+    value = kv_all / (ms_per_step * 1e-3) / 1e9
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    tflops = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    attn_avg = statistics.mean(attn_ms)
+    attn_gbs = alg["attn_bytes"] / (attn_avg * 1e-3) / 1e9
+    attn_tfs = alg["flops"] / (attn_avg * 1e-3) / 1e12
+    t_roof_ms = max(alg["step_bytes"] / (hbm * 1e9), alg["flops"] / (tflops * 1e12)) * 1e3
+    bound = "hbm" if alg["attn_bytes"] / hbm >= alg["flops"] / (tflops * 1e3) else "tensor"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(attn_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(attn_gbs / hbm, 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(attn_tfs, 1), "peak": tflops,
+                "unit": "TFLOP/s", "frac": round(attn_tfs / tflops, 4)}
+    roof.update({"traffic": None, "peak_source": f"{peak_src} (MEASURED_PEAKS.json)"
+                 if peak_src == "measured" else "fallback",
+                 "kernel": "dcp_decode_attn", "attn_ms": round(attn_avg, 4),
+                 "merge_ms": round(statistics.mean(merge_ms), 4),
+                 "alg_bytes_per_launch": alg["attn_bytes"], "alg_flops_per_launch": alg["flops"],
+                 "step_frac_of_roofline": round(t_roof_ms / (ms_per_step), 4)})
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; log-normal lengths stand in for the blog's agentic trace)",
+        "config": {"workload": w.name, "kind": w.kind, "batch": B, "q_len": Lq,
+                   "num_q_heads": Hq, "num_kv_heads": w.num_kv_heads,
+                   "head_dim_qk": w.head_dim_qk, "head_dim_v": Dv, "block_size": w.block_size,
+                   "dcp_size": N, "interleave": w.interleave,
+                   "kv_tokens": alg["tokens"], "kv_bytes": alg["kv_bytes"],
+                   "l2": "inputs larger than L2 (cache resident, no flush)"
+                   if alg["kv_bytes"] > 4 * 129e6 else "L2 flushed between steps",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "query_tokens_per_s": round(qtok_all / (ms_per_step * 1e-3), 1),
+        "roofline": roof,
+        "clocks": clocks.summary(),
+        "e2e": {"value": round(kv_all / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, kvb, nseq, qtok = oracle_time(inst, args.cpu_budget, args.cpu_max_seqs)
+        result["cpu_baseline"] = {
+            "value": round(kvb / secs / 1e9, 4), "unit": "GB/s", "cores": cpu_threads(),
+            "kind": "oracle",
+            "sample": f"{nseq} request(s) of {w.name} ({kvb / 1e9:.2f} GB of cache, all "
+                      f"{w.dcp_size} shards + merge), numpy fp64, {secs:.1f} s",
+            "query_tokens_per_s": round(qtok / secs, 4)}
+    if world > 1:
+        import torch.distributed as td
+        td.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def run_reference(args):
+    """The CPU oracle on the host cores, timed as the reference arm."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = wl.WORKLOADS[args.workload]
+    if torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    inst = setup_reference_inputs(w)
+    budget = max(2.0, args.cpu_budget / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_time(inst, budget, args.cpu_max_seqs)
+    secs = kvb = qtok = 0
+    nseq = 0
+    for _ in range(args.steps):
+        s, k, n, qt = oracle_time(inst, budget, args.cpu_max_seqs)
+        secs += s
+        kvb += k
+        nseq += n
+        qtok += qt
+    value = kvb / secs / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "kind": w.kind, "batch": w.batch, "q_len": w.q_len,
+                   "dcp_size": w.dcp_size, "interleave": w.interleave},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cpu_threads(),
+                         "kind": "oracle",
+                         "sample": f"{nseq} request(s) of {w.name} over {args.steps} steps "
+                                   f"({kvb / 1e9:.2f} GB of cache)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def setup_reference_inputs(w):
+    """Same seeded workload as the GPU leg, block counts from the oracle."""
+    from oracle import dcp_oracle as orc
+    seq_lens = wl.make_seq_lens(w)
+    lnb = np.zeros((w.dcp_size, w.batch), dtype=np.int32)
+    for b, S in enumerate(seq_lens.tolist()):
+        for r, toks in enumerate(orc.shard_token_lists(S, w.interleave, w.dcp_size)):
+            lnb[r, b] = -(-len(toks) // w.block_size)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    return wl.make_instance(w, lnb, device=dev, seq_lens=seq_lens)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mla_512", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle time for the CPU baseline sample")
+    ap.add_argument("--cpu-max-seqs", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,61 @@
+// Internal interface between the C-ABI layer (dcp_api.cu) and the kernel
+// translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dcp.h"
+
+namespace dcp {
+
+// Everything a decode-attention kernel needs, validated by the API layer.
+struct AttnArgs {
+  int kind;              // DCP_ATTN_GQA / DCP_ATTN_MLA
+  int B, Lq, Hq, Hkv, Dqk, Dv, bs, num_blocks, max_lb;
+  int N, I;              // dcp_size, interleave
+  float scale;
+  const void* q;         // bf16 [B][Lq][Hq][Dqk]
+  const void* kv;        // bf16 cache (see dcp.h)
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  float* partial_out;    // fp32 [N][B][Lq][Hq][Dv]
+  float* lse;            // fp32 [N][B][Lq][Hq]
+  void* workspace;
+  size_t workspace_bytes;
+  int* status;           // device status word
+  cudaStream_t stream;
+};
+
+// How a call is cut into work units along the local KV axis.
+struct SplitPlan {
+  int n_split;           // KV splits per (shard, request[, query]) unit
+  int split_tokens;      // local tokens per split (multiple of the kernel tile)
+  size_t ws_bytes;       // workspace for split partials (0 when n_split == 1)
+};
+
+// Workspace layout when n_split > 1:
+//   ws_o   fp32 [N][B][Lq][n_split][Hq][Dv]
+//   ws_lse fp32 [N][B][Lq][n_split][Hq]       (after ws_o, 256-byte aligned)
+SplitPlan plan_splits(const AttnArgs& a, int sm_count, int tile_tokens, int units_per_split);
+
+int device_sm_count();
+
+// Launchers; each returns a cudaError_t from the launch.
+cudaError_t launch_slot_map(const int32_t* seq_lens, int B, int bs, int I, int N,
+                            int32_t* local_seq_lens, int32_t* local_num_blocks,
+                            int32_t* shard_of, int32_t* local_pos, int max_seq, int* status,
+                            cudaStream_t stream);
+
+cudaError_t launch_merge(const float* partial_out, const float* lse, int N, int B, int Lq,
+                         int Hq, int Dv, void* out, float* out_lse, cudaStream_t stream);
+
+// Combine n_split workspace partials into partial_out / lse (row a5).
+cudaError_t launch_split_combine(const AttnArgs& a, const SplitPlan& p);
+
+// Generic SIMT kernel (any head dims); used for shapes the tensor-core kernels
+// do not take.
+cudaError_t launch_attn_simt(const AttnArgs& a, const SplitPlan& p);
+SplitPlan plan_attn_simt(const AttnArgs& a, int sm_count);
+
+}  // namespace dcp

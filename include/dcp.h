@@ -1,0 +1,170 @@
+/*
+ * dcp.h - C ABI of libdcp: Decode Context Parallelism (DCP) decode attention
+ * for one GB300 (sm_103a).
+ *
+ * What the library computes (vLLM Decode Context Parallelism blog, agentlenshq,
+ * zh-TW, sections "解碼上下文並行 (DCP) 原理解析" and "DCP 執行流程"): the paged KV
+ * cache of each request is split along the sequence into dcp_size shards; the
+ * full query attends to each shard's keys alone, giving a partial output and
+ * its log-sum-exp (LSE); the partials are merged by LSE reweighting (the
+ * online-softmax rule) and each shard index r receives the slice of heads it
+ * owns.  On one GPU the shards are partitions of one device pool and the
+ * "exchange" is a device buffer read by dcp_merge.
+ *
+ * Token -> shard rule (the interleave flag cp_kv_cache_interleave_size of the
+ * vLLM Ascend "Context Parallel Guide", section "Decode Context Parallel"):
+ *     shard(t) = (t / interleave) % dcp_size
+ *     local(t) = (t / (interleave * dcp_size)) * interleave + t % interleave
+ * Tokens of one shard are stored densely in increasing global order.
+ *
+ * Conventions for every call
+ *  - Pointers are DEVICE pointers owned by the caller unless stated otherwise.
+ *    The library never allocates, frees or keeps them.
+ *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream.  Work is enqueued on it; no call synchronises the host except
+ *    dcp_get_last_device_status.
+ *  - Arguments are checked on the host first; a bad argument returns an error
+ *    code and launches nothing.  Errors found on the device (a sequence shorter
+ *    than its query, a block id out of range, a bounded wait that expired) set a
+ *    device status word read by dcp_get_last_device_status; the kernels then
+ *    skip the offending work unit.
+ *  - No C++ exception crosses this interface.
+ *  - Integer tensors are int32, row-major (C order), without padding.
+ */
+#ifndef DCP_H_
+#define DCP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DCP_API __attribute__((visibility("default")))
+#else
+#define DCP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DCP_OK = 0,
+  DCP_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or shape          */
+  DCP_ERR_UNSUPPORTED = 2,  /* valid request this build has no kernel for     */
+  DCP_ERR_CUDA = 3,         /* a CUDA runtime call failed                      */
+  DCP_ERR_TIMEOUT = 4,      /* a device-side bounded wait expired              */
+  DCP_ERR_BOUNDS = 5        /* device-side range check failed (see above)     */
+} dcp_status_t;
+
+typedef enum { DCP_ATTN_GQA = 0, DCP_ATTN_MLA = 1 } dcp_attn_kind_t;
+
+/* Shape of one decode-attention call.
+ *  kind            DCP_ATTN_GQA or DCP_ATTN_MLA
+ *  batch           B, number of requests
+ *  q_len           Lq, query tokens per request (1 = plain decode; 4 = MTP
+ *                  verify with 3 speculative tokens, causal within the Lq)
+ *  num_q_heads     Hq
+ *  num_kv_heads    Hkv (MLA: 1); query head h reads KV head h / (Hq / Hkv)
+ *  head_dim_qk     Dqk (MLA: 576 = 512 latent + 64 rope)
+ *  head_dim_v      Dv  (MLA: 512, the value is the first Dv entries of the row)
+ *  block_size      tokens per cache block
+ *  num_blocks      blocks in the cache pool (block ids are < num_blocks)
+ *  max_local_blocks  third dimension of block_tables                       */
+typedef struct {
+  int32_t kind;
+  int32_t batch;
+  int32_t q_len;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim_qk;
+  int32_t head_dim_v;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t max_local_blocks;
+} dcp_attn_desc_t;
+
+/* Step a1: the token -> shard map.
+ * Source: DCP principle section of the vLLM DCP blog (each rank holds a range
+ * of token positions; worked example 200K tokens on 4 ranks) and the interleave
+ * flag of the vLLM Ascend Context Parallel Guide.
+ *  seq_lens          [B]            context length of each request
+ *  local_seq_lens    [dcp][B] out   tokens held by shard r
+ *  local_num_blocks  [dcp][B] out   ceil(local_seq_lens / block_size)
+ *  shard_of, local_pos  [B][max_seq] out, optional (both NULL or both set):
+ *                    owning shard and shard-local index of token t, -1 for
+ *                    t >= seq_lens[b]
+ *  max_seq           row length of shard_of/local_pos (ignored when NULL)
+ * Errors: INVALID_ARG for batch < 0, block_size/interleave/dcp_size < 1, NULL
+ * required pointers, exactly one of shard_of/local_pos NULL, max_seq < 1 with
+ * the maps requested.  A seq_len < 0 sets DCP_ERR_BOUNDS on the device.      */
+DCP_API dcp_status_t dcp_build_slot_map(const int32_t* seq_lens, int32_t batch, int32_t block_size,
+                                int32_t interleave, int32_t dcp_size,
+                                int32_t* local_seq_lens, int32_t* local_num_blocks,
+                                int32_t* shard_of, int32_t* local_pos, int32_t max_seq,
+                                void* stream);
+
+/* Bytes of device scratch dcp_decode_attn needs for this shape (0 is
+ * possible).  Depends on the shape only (not on the contents of seq_lens).
+ * Returns 0 and sets nothing for an invalid descriptor. */
+DCP_API size_t dcp_decode_attn_workspace_size(const dcp_attn_desc_t* d, int32_t dcp_size);
+
+/* Steps a2-a5: per-shard partial attention with LSE.
+ * Source: "DCP 執行流程" of the vLLM DCP blog: the full query (AllGather Q)
+ * attends to the shard's local KV slice only (Compute).
+ * For shard r, request b, query i (position p = seq_lens[b] - Lq + i), head h:
+ *   s_t = scale * q[b][i][h] . k_t  over the keys t of shard r with t <= p
+ *   lse[r][b][i][h]         = log sum_t exp(s_t)               (natural log)
+ *   partial_out[r][b][i][h] = sum_t exp(s_t - lse) * v_t
+ * A shard with no visible key gives partial_out = 0 and lse = -inf.
+ *  q             bf16 [B][Lq][Hq][Dqk]
+ *  kv_cache      bf16, GQA [2][num_blocks][block_size][Hkv][Dqk] (K pool, then
+ *                V pool; requires Dv == Dqk); MLA [num_blocks][block_size][Dqk]
+ *  block_tables  [dcp][B][max_local_blocks]: shard r's j-th local token of
+ *                request b is at block block_tables[r][b][j / block_size],
+ *                slot j % block_size
+ *  seq_lens      [B], each >= Lq (checked on the device)
+ *  causal_q_len  must equal d->q_len
+ *  partial_out   fp32 [dcp][B][Lq][Hq][Dv] out;  lse fp32 [dcp][B][Lq][Hq] out
+ *  workspace     >= dcp_decode_attn_workspace_size(d, dcp_size) bytes, 256-byte
+ *                aligned (may be NULL when that size is 0); its contents on entry
+ *                do not matter
+ * Alignment: q, kv_cache, partial_out 16 bytes.
+ * Errors: INVALID_ARG (NULL pointers, sizes < 1, Hq % Hkv != 0, MLA with
+ * Hkv != 1 or Dv > Dqk, GQA with Dv != Dqk, causal_q_len != q_len, small
+ * workspace, misalignment); UNSUPPORTED (head dims without a kernel); CUDA.  */
+DCP_API dcp_status_t dcp_decode_attn(const dcp_attn_desc_t* d, const void* q, const void* kv_cache,
+                             const int32_t* block_tables, const int32_t* seq_lens,
+                             int32_t dcp_size, int32_t interleave, float scale,
+                             int32_t causal_q_len, float* partial_out, float* lse,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Step a6: LSE merge and head-slice return.
+ * Source: "DCP 執行流程" of the vLLM DCP blog, AllGather + ReduceScatter: the
+ * partials and LSEs are shared, reweighted with the online-softmax rule and
+ * summed, and each rank gets only its head slice.
+ *   LSE = m + log sum_r exp(lse_r - m),  m = max_r lse_r
+ *   o   = sum_r exp(lse_r - LSE) * partial_out_r
+ * out[r][b][i][h'] = o[b][i][r * Hq/dcp + h'] (bf16, round to nearest even).
+ * All shards -inf gives out = 0 and out_lse = -inf.
+ *  partial_out fp32 [dcp][B][Lq][Hq][Dv], lse fp32 [dcp][B][Lq][Hq]
+ *  out     bf16 [dcp][B][Lq][Hq/dcp][Dv] out
+ *  out_lse fp32 [dcp][B][Lq][Hq/dcp] out, optional (NULL to skip)
+ * Alignment: partial_out 16 bytes, out 8 bytes; Dv % 4 == 0.
+ * Errors: INVALID_ARG (NULL, sizes < 1, Hq % dcp != 0 - the one-GPU form of
+ * the pages' TP/DCP divisibility constraints -, Dv % 4 != 0, alignment).     */
+DCP_API dcp_status_t dcp_merge(const float* partial_out, const float* lse, int32_t dcp_size,
+                       int32_t batch, int32_t q_len, int32_t num_q_heads, int32_t head_dim_v,
+                       void* out, float* out_lse, void* stream);
+
+/* Synchronises `stream`, returns the device status word set by earlier kernels
+ * (DCP_OK if none) and clears it. */
+DCP_API dcp_status_t dcp_get_last_device_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+DCP_API const char* dcp_status_string(dcp_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DCP_H_ */

@@ -1,0 +1,124 @@
+"""C ABI checks that need no GPU: the library loads, exports every declared
+symbol, and rejects bad arguments on the host before any launch."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dcp.h")
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    return re.findall(r"DCP_API[^;(]*?\b(dcp_\w+)\s*\(", src)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from context_decode_attention_paged_gb300 import build
+    build.build()
+    from context_decode_attention_paged_gb300 import binding
+    return binding
+
+
+def test_header_declares_the_calls():
+    syms = declared_symbols()
+    for s in ("dcp_build_slot_map", "dcp_decode_attn", "dcp_merge",
+              "dcp_decode_attn_workspace_size", "dcp_get_last_device_status",
+              "dcp_status_string"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = lib.raw_lib()
+    for s in declared_symbols():
+        assert hasattr(raw, s), s
+
+
+def test_status_strings(lib):
+    assert lib.status_string(0) == "DCP_OK"
+    assert lib.status_string(1) == "DCP_ERR_INVALID_ARG"
+    assert lib.status_string(5) == "DCP_ERR_BOUNDS"
+    assert lib.status_string(99) == "DCP_ERR_UNKNOWN"
+
+
+FAKE = ctypes.c_void_p(0x10000)   # 256-byte aligned, never dereferenced: the calls below
+                                  # must fail validation before touching memory
+
+
+def _attn(lib, desc, dcp_size=2, interleave=16, scale=0.125, causal=None, q=FAKE, kv=FAKE,
+          po=FAKE):
+    raw = lib.raw_lib()
+    return raw.dcp_decode_attn(ctypes.byref(desc), q, kv, FAKE, FAKE, dcp_size, interleave,
+                               scale, desc.q_len if causal is None else causal, po, FAKE, FAKE,
+                               0, None)
+
+
+def _desc(lib, **kw):
+    base = dict(kind="gqa", batch=1, q_len=1, num_q_heads=8, num_kv_heads=2, head_dim_qk=64,
+                head_dim_v=64, block_size=16, num_blocks=64, max_local_blocks=32)
+    base.update(kw)
+    return lib.make_desc(**base)
+
+
+@pytest.mark.parametrize("kw,extra", [
+    (dict(num_q_heads=7), {}),                      # Hq % Hkv != 0
+    (dict(batch=0), {}),
+    (dict(q_len=0), {}),
+    (dict(block_size=0), {}),
+    (dict(kind=7), {}),
+    (dict(kind="mla", num_kv_heads=2), {}),         # MLA has one latent head
+    (dict(kind="mla", num_kv_heads=1, head_dim_v=600, head_dim_qk=576), {}),
+    (dict(head_dim_v=32), {}),                      # GQA needs Dv == Dqk
+    ({}, dict(dcp_size=0)),
+    ({}, dict(dcp_size=33)),
+    ({}, dict(interleave=0)),
+    ({}, dict(scale=0.0)),
+    ({}, dict(causal=2)),                           # causal_q_len must equal q_len
+    ({}, dict(q=ctypes.c_void_p(0x10002))),         # misaligned q
+    ({}, dict(kv=ctypes.c_void_p(0x10008))),        # misaligned cache
+    ({}, dict(q=None)),
+])
+def test_decode_attn_rejects_bad_arguments(lib, kw, extra):
+    assert _attn(lib, _desc(lib, **kw), **extra) == lib.DCP_ERR_INVALID_ARG
+
+
+def test_decode_attn_unsupported_head_dim(lib):
+    assert _attn(lib, _desc(lib, head_dim_qk=60, head_dim_v=60)) == lib.DCP_ERR_UNSUPPORTED
+
+
+def test_merge_rejects_bad_arguments(lib):
+    raw = lib.raw_lib()
+    ok = dict(N=2, B=1, Lq=1, Hq=8, Dv=64)
+
+    def call(N, B, Lq, Hq, Dv, po=FAKE, out=FAKE):
+        return raw.dcp_merge(po, FAKE, N, B, Lq, Hq, Dv, out, None, None)
+
+    assert call(**{**ok, "Hq": 6, "N": 4}) == lib.DCP_ERR_INVALID_ARG   # Hq % N != 0
+    assert call(**{**ok, "Dv": 62}) == lib.DCP_ERR_INVALID_ARG
+    assert call(**{**ok, "N": 0}) == lib.DCP_ERR_INVALID_ARG
+    assert call(**{**ok, "B": 0}) == lib.DCP_ERR_INVALID_ARG
+    assert call(**ok, po=ctypes.c_void_p(0x10004)) == lib.DCP_ERR_INVALID_ARG
+    assert call(**ok, out=None) == lib.DCP_ERR_INVALID_ARG
+
+
+def test_slot_map_rejects_bad_arguments(lib):
+    raw = lib.raw_lib()
+    assert raw.dcp_build_slot_map(FAKE, 1, 0, 16, 2, FAKE, FAKE, None, None, 0, None) == 1
+    assert raw.dcp_build_slot_map(FAKE, 1, 16, 0, 2, FAKE, FAKE, None, None, 0, None) == 1
+    assert raw.dcp_build_slot_map(FAKE, 1, 16, 16, 0, FAKE, FAKE, None, None, 0, None) == 1
+    assert raw.dcp_build_slot_map(FAKE, -1, 16, 16, 2, FAKE, FAKE, None, None, 0, None) == 1
+    assert raw.dcp_build_slot_map(FAKE, 1, 16, 16, 2, FAKE, FAKE, FAKE, None, 8, None) == 1
+    assert raw.dcp_build_slot_map(FAKE, 1, 16, 16, 2, FAKE, FAKE, FAKE, FAKE, 0, None) == 1
+    assert raw.dcp_build_slot_map(None, 1, 16, 16, 2, FAKE, FAKE, None, None, 0, None) == 1
+    # an empty batch is a no-op success
+    assert raw.dcp_build_slot_map(None, 0, 16, 16, 2, None, None, None, None, 0, None) == 0
+
+
+def test_workspace_size_of_invalid_desc_is_zero(lib):
+    assert lib.dcp_decode_attn_workspace_size(_desc(lib, num_q_heads=7), 2) == 0

@@ -1,0 +1,113 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Sizes are small enough for the oracle to finish in seconds but span several
+kernel tiles and a ragged tail; edge cases cover empty shards, a single token,
+seq_len == q_len, interleave 1 and interleave >= seq_len.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import helpers as H
+from gpu_common import check_against_oracle, run_gpu
+from oracle import dcp_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from context_decode_attention_paged_gb300 import build
+    build.build()
+
+
+# ---------------------------------------------------------------------------
+# a1: slot map, bit-exact
+# ---------------------------------------------------------------------------
+
+SLOT_CASES = [
+    ([1024], 16, 2, 16),
+    ([1, 2, 3, 17, 128, 129, 1000], 16, 2, 16),
+    ([200000], 1, 8, 128),
+    ([200000], 50000, 4, 128),
+    ([5, 300, 64], 1000, 4, 16),
+    ([8192, 32768, 12345], 128, 4, 128),
+    ([0, 7, 4096], 7, 3, 5),
+]
+
+
+@pytest.mark.parametrize("lens,I,N,bs", SLOT_CASES)
+def test_slot_map_bit_exact(lens, I, N, bs):
+    from context_decode_attention_paged_gb300 import binding as dcp
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    max_seq = max(lens) + 3
+    lsl, lnb, shard, local = dcp.dcp_build_slot_map(sl, bs, I, N, max_seq=max_seq)
+    torch.cuda.synchronize()
+    assert dcp.dcp_get_last_device_status() == dcp.DCP_OK
+    ref = orc.ref_slot_map(lens, I, N, bs)
+    assert np.array_equal(lsl.cpu().numpy(), ref["local_seq_lens"])
+    assert np.array_equal(lnb.cpu().numpy(), ref["local_num_blocks"])
+    rs = np.full((len(lens), max_seq), -1, dtype=np.int32)
+    rl = np.full((len(lens), max_seq), -1, dtype=np.int32)
+    rs[:, : ref["shard_of"].shape[1]] = ref["shard_of"]
+    rl[:, : ref["local_pos"].shape[1]] = ref["local_pos"]
+    assert np.array_equal(shard.cpu().numpy(), rs)
+    assert np.array_equal(local.cpu().numpy(), rl)
+
+
+def test_slot_map_negative_len_sets_bounds_status():
+    from context_decode_attention_paged_gb300 import binding as dcp
+    sl = torch.tensor([5, -3], dtype=torch.int32, device="cuda")
+    lsl, lnb, _, _ = dcp.dcp_build_slot_map(sl, 16, 4, 2)
+    assert dcp.dcp_get_last_device_status() == dcp.DCP_ERR_BOUNDS
+    assert lsl.cpu()[:, 1].tolist() == [0, 0]
+    assert dcp.dcp_get_last_device_status() == dcp.DCP_OK   # cleared by the read
+
+
+# ---------------------------------------------------------------------------
+# a3-a6: attention + merge
+# ---------------------------------------------------------------------------
+
+ATTN_CASES = [
+    ("tiny_gqa", {}),                                                  # the full tiny config
+    ("tiny_gqa", dict(batch=3, lengths=("uniform", 1, 700), dcp_size=4, interleave=3)),
+    ("tiny_gqa", dict(lengths=("fixed", 40), dcp_size=4, interleave=64)),   # empty shards
+    ("tiny_gqa", dict(batch=2, q_len=3, lengths=("uniform", 3, 300))),      # causal Lq=3
+    ("tiny_gqa", dict(lengths=("fixed", 1))),                               # single token
+    ("qwen_gqa", dict(batch=2, lengths=("uniform", 300, 2000), dcp_size=4)),
+    ("qwen_gqa", dict(batch=1, q_len=2, lengths=("fixed", 1153), dcp_size=2, interleave=1)),
+    ("mla_32", dict(batch=2, lengths=("uniform", 900, 3000))),
+    ("mla_32", dict(batch=1, lengths=("fixed", 129), dcp_size=2, interleave=128)),
+    ("mla_mtp", dict(lengths=("fixed", 2500))),
+    ("mla_mtp", dict(lengths=("fixed", 4))),                                # S == Lq
+    ("mla_mtp", dict(lengths=("fixed", 300), dcp_size=1)),
+]
+
+
+@pytest.mark.parametrize("name,kw", ATTN_CASES)
+def test_attention_matches_oracle(name, kw):
+    inst = H.build_instance(H.small(name, **kw))
+    check_against_oracle(inst)
+
+
+@pytest.mark.parametrize("N", [1, 2, 4, 8])
+def test_mtp_merge_invariance_sweep(N):
+    """MTP verify (Lq 4, interleave 1): merged output equals the oracle at every dcp_size."""
+    w = H.small("mla_mtp", lengths=("fixed", 1500), dcp_size=N)
+    check_against_oracle(H.build_instance(w))
+
+
+def test_seq_shorter_than_query_sets_bounds_status():
+    from context_decode_attention_paged_gb300 import binding as dcp
+    w = H.small("tiny_gqa", batch=2, q_len=4, lengths=("fixed", 64))
+    inst = H.build_instance(w)
+    inst.seq_lens[1] = 2                       # shorter than its 4 query tokens
+    got = run_gpu(inst)
+    assert got["status"] == dcp.DCP_ERR_BOUNDS
+    assert (got["lse"][:, 1] == -np.inf).all()
+    assert np.isfinite(got["lse"][:, 0]).all()
