@@ -1,0 +1,454 @@
+// Step a4: per-shard partial attention for MLA (one shared latent KV head of
+// 576 = 512 latent + 64 rope values; the value is the first 512), on tcgen05
+// tensor cores.
+//
+// vLLM DCP blog, "DCP 執行流程", Compute step (each shard attends the full
+// query to its local KV slice and returns a partial output with its LSE) and
+// section "Multi-head Latent Attention (MLA) 後端" (one low-rank latent KV head
+// shared by every query head).
+//
+// Work unit = (shard r, request b, query i, KV split s), run by a cluster of
+// two CTAs.  With 128 query heads the fp32 output (128 x 512) fills a whole
+// SM's tensor memory and the bf16 query (128 x 576) does not fit next to a KV
+// ring in shared memory, so the pair splits the head dimensions:
+//   CTA c holds query dims D_c = latent[256c, 256c+256) + rope[32c, 32c+32) in
+//   TMEM, streams the same dims of each 64-token KV tile (TMA, 128B/64B
+//   swizzle) and computes the partial score S_c = Q_c K_c^T (M=128 heads, N=64
+//   tokens, K=288; A from TMEM).  The two CTAs swap S_c through distributed
+//   shared memory, so both hold S = S_0 + S_1 (bit-identical: fp32 addition
+//   commutes) and run the same online softmax.  CTA c then accumulates output
+//   dims [256c, 256c+256) = O_c += P V_c (M=128, N=256, K=64; P from TMEM, V
+//   read MN-major from the latent part of its own KV tile).
+// Every KV byte is loaded once (each CTA loads its half of the dims) and no MMA
+// is repeated.  The softmax runs in the log2 domain with a lazily updated
+// reference max (rescale O only when the running max grows by more than 2^8).
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
+// owner, warps 2..5 = softmax/epilogue, one query head (TMEM lane) per thread.
+// Every wait is bounded; on expiry the kernel records DCP_ERR_TIMEOUT, drains
+// its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "dcp_device.cuh"
+#include "dcp_internal.h"
+#include "dcp_sm100.cuh"
+#include "dcp_tma.h"
+
+namespace dcp {
+namespace {
+
+using namespace sm100;
+
+constexpr int kHeads = 128;
+constexpr int kDqk = 576, kDv = 512, kLatent = 512;
+constexpr int kNt = 64;                       // tokens per KV tile (half a 128-token block)
+constexpr int kStages = 5;
+constexpr uint32_t kChunkBytes = kNt * 128;   // 64 tokens x 64 dims bf16, 128B rows
+constexpr uint32_t kRopeBytes = kNt * 64;     // 64 tokens x 32 dims bf16, 64B rows
+constexpr uint32_t kStageBytes = 4 * kChunkBytes + kRopeBytes;   // 36 KB
+constexpr uint32_t kXRowFloats = 68;          // exchange row: 64 scores + pad (bank spread)
+constexpr uint32_t kXBytes = kHeads * kXRowFloats * 4;
+constexpr uint32_t kThreads = 192;
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
+// TMEM columns
+constexpr uint32_t kColQ = 0;      // 144 cols: 128 rows x 288 bf16
+constexpr uint32_t kColP = 144;    // 32 cols: 128 rows x 64 bf16
+constexpr uint32_t kColS = 192;    // 64 cols fp32
+constexpr uint32_t kColO = 256;    // 256 cols fp32
+constexpr float kRescaleLog2 = 8.0f;
+
+struct MlaParams {
+  const __nv_bfloat16* q;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  float* dst_o;        // partial_out, or the split workspace
+  float* dst_lse;
+  int* status;
+  int B, Lq, N, I, max_lb, bs, num_blocks, n_split, split_tokens;
+  float scale_log2;    // scale * log2(e)
+};
+
+struct Smem {
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full, s_free, p_full, pv_done, recv_full, sent_free, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
+                const MlaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = base;                                        // kStages x 36 KB
+  float* xbuf = reinterpret_cast<float*>(base + kStages * kStageBytes);   // peer's scores land here
+  Smem& sm = *reinterpret_cast<Smem*>(base + kStages * kStageBytes + kXBytes);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t cta = cluster_ctarank();          // 0 or 1
+  const uint32_t peer = cta ^ 1u;
+  const long long unit = blockIdx.x >> 1;
+  const int s_idx = (int)(unit % p.n_split);
+  const int i_q = (int)((unit / p.n_split) % p.Lq);
+  const int b = (int)((unit / ((long long)p.n_split * p.Lq)) % p.B);
+  const int r = (int)(unit / ((long long)p.n_split * p.Lq * p.B));
+
+  // key range of this unit (shard-local indices [kb, ke))
+  const int S = p.seq_lens[b];
+  const bool bad_len = S < p.Lq;
+  int L = bad_len ? 0 : local_len(S, r, p.I, p.N);
+  const bool short_table = (long long)L > (long long)p.max_lb * p.bs;
+  if (short_table) L = p.max_lb * p.bs;
+  const int vis = bad_len ? 0 : min(L, local_count_upto((long long)S - p.Lq + i_q, r, p.I, p.N));
+  const int kb = min(vis, s_idx * p.split_tokens);
+  const int ke = min(vis, kb + p.split_tokens);
+  const int T = (ke - kb + kNt - 1) / kNt;
+  if (tid == 0 && cta == 0 && (bad_len || short_table)) set_status(p.status, DCP_ERR_BOUNDS);
+
+  if (tid == 0) {
+    for (int k = 0; k < kStages; ++k) {
+      mbar_init(smem_u32(&sm.kv_full[k]), 1);
+      mbar_init(smem_u32(&sm.kv_empty[k]), 1);
+    }
+    mbar_init(smem_u32(&sm.s_full), 1);
+    mbar_init(smem_u32(&sm.s_free), 128);
+    mbar_init(smem_u32(&sm.p_full), 128);
+    mbar_init(smem_u32(&sm.pv_done), 1);
+    mbar_init(smem_u32(&sm.recv_full), 128);
+    mbar_init(smem_u32(&sm.sent_free), 128);
+    mbar_init(smem_u32(&sm.drain), 1);
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&sm.tmem_base), 512);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  // query slice of this CTA -> TMEM (row = head = TMEM lane, bf16 pairs per column)
+  if (warp >= 2) {
+    const int h = (warp & 3) * 32 + lane;
+    const uint4* qrow = reinterpret_cast<const uint4*>(
+        p.q + (((long long)b * p.Lq + i_q) * kHeads + h) * kDqk);
+    const uint32_t lane_addr = taddr(tmem, (uint32_t)((warp & 3) * 32), 0);
+#pragma unroll
+    for (int c = 0; c < 9; ++c) {          // 9 x 16 columns = 288 dims
+      uint32_t v[16];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        // column block c covers dims [32c, 32c+32) of the slice: latent 256*cta + 32c
+        // for c < 8, rope 512 + 32*cta for c == 8; 8 bf16 per uint4
+        const int dim0 = (c < 8) ? (256 * (int)cta + 32 * c) : (kLatent + 32 * (int)cta);
+        const uint4 w = __ldg(qrow + dim0 / 8 + k);
+        v[4 * k + 0] = w.x;
+        v[4 * k + 1] = w.y;
+        v[4 * k + 2] = w.z;
+        v[4 * k + 3] = w.w;
+      }
+      tmem_st16(lane_addr + kColQ + 16 * c, v);
+    }
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  cluster_sync();            // barriers of both CTAs initialised, query staged
+  tc_fence_after();
+
+  volatile int* abort_flag = &sm.abort;
+  auto fail = [&](void) {
+    set_status(p.status, DCP_ERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0 && T > 0) {
+      prefetch_tmap(&tm_lat);
+      prefetch_tmap(&tm_rope);
+      const int32_t* bt = p.block_tables + ((long long)r * p.B + b) * p.max_lb;
+      int next_blk = bt[kb / 128];
+      int issued[kStages];
+#pragma unroll
+      for (int k = 0; k < kStages; ++k) issued[k] = 0;
+      for (int t = 0; t < T; ++t) {
+        const int j = kb + t * kNt;
+        const int blk = next_blk;
+        if (t + 1 < T) next_blk = bt[(j + kNt) / 128];
+        const int st = t % kStages;
+        const uint32_t ph = (uint32_t)(t / kStages) & 1u;
+        if (*abort_flag || !mbar_wait(smem_u32(&sm.kv_empty[st]), ph ^ 1u, kWaitNs)) {
+          fail();
+          break;
+        }
+        if ((unsigned)blk >= (unsigned)p.num_blocks) set_status(p.status, DCP_ERR_BOUNDS);
+        const int row = blk * 128 + (j & 127);   // out-of-range rows read as zeros
+        const uint32_t full = smem_u32(&sm.kv_full[st]);
+        uint8_t* dst = stages + st * kStageBytes;
+        mbar_arrive_expect_tx(full, kStageBytes);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tma_load_2d(smem_u32(dst + c * kChunkBytes), &tm_lat, 256 * (int)cta + 64 * c, row, full);
+        tma_load_2d(smem_u32(dst + 4 * kChunkBytes), &tm_rope, kLatent + 32 * (int)cta, row, full);
+        ++issued[st];
+      }
+      if (*abort_flag) {
+        // let every copy this thread issued land before the CTA exits
+        for (int k = 0; k < kStages; ++k)
+          if (issued[k] > 0)
+            mbar_wait(smem_u32(&sm.kv_full[k]), (uint32_t)(issued[k] - 1) & 1u, kWaitNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0 && T > 0) {
+      const uint32_t id_qk = idesc_bf16(128, kNt, false);
+      const uint32_t id_pv = idesc_bf16(128, 256, true);
+      auto issue_pv = [&](int t) -> bool {
+        if (*abort_flag || !mbar_wait(smem_u32(&sm.p_full), (uint32_t)t & 1u, kWaitNs)) return false;
+        tc_fence_after();
+        const uint8_t* st = stages + (t % kStages) * kStageBytes;
+#pragma unroll
+        for (int k = 0; k < kNt / 16; ++k) {
+          const uint64_t bdesc = smem_desc(smem_u32(st + k * 2048), kChunkBytes, 1024, kSw128);
+          mma_ts(tmem + kColO, tmem + kColP + 8 * k, bdesc, id_pv, (t > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&sm.pv_done));
+        mma_commit(smem_u32(&sm.kv_empty[t % kStages]));
+        return true;
+      };
+      bool ok = true;
+      for (int t = 0; t < T && ok; ++t) {
+        const int st = t % kStages;
+        if (*abort_flag || !mbar_wait(smem_u32(&sm.kv_full[st]), (uint32_t)(t / kStages) & 1u, kWaitNs) ||
+            (t > 0 && !mbar_wait(smem_u32(&sm.s_free), (uint32_t)(t - 1) & 1u, kWaitNs))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t* sb = stages + st * kStageBytes;
+#pragma unroll
+        for (int k = 0; k < 18; ++k) {
+          const uint64_t bdesc =
+              (k < 16) ? smem_desc(smem_u32(sb + (k >> 2) * kChunkBytes + (k & 3) * 32), 16, 1024, kSw128)
+                       : smem_desc(smem_u32(sb + 4 * kChunkBytes + (k - 16) * 32), 16, 512, kSw64);
+          mma_ts(tmem + kColS, tmem + kColQ + 8 * k, bdesc, id_qk, k > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&sm.s_full));
+        if (t > 0) ok = issue_pv(t - 1);
+      }
+      if (ok) ok = issue_pv(T - 1);
+      if (!ok) fail();
+      // drain: arrives when every MMA issued above has completed
+      mma_commit(smem_u32(&sm.drain));
+      if (!mbar_wait(smem_u32(&sm.drain), 0, kWaitNs)) fail();
+    }
+  } else {
+    // ---------------- softmax / epilogue (warps 2..5) ----------------
+    const int lg = warp & 3;                       // TMEM lane group
+    const int h = lg * 32 + lane;                  // query head = TMEM lane
+    const uint32_t lane_addr = taddr(tmem, (uint32_t)(lg * 32), 0);
+    const uint32_t my_x = smem_u32(xbuf + h * kXRowFloats);
+    const uint32_t peer_x = mapa(my_x, peer);
+    const uint32_t peer_recv_full = mapa(smem_u32(&sm.recv_full), peer);
+    const uint32_t peer_sent_free = mapa(smem_u32(&sm.sent_free), peer);
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    // waits and the abort flag are made warp-uniform: the tcgen05 ld/st below
+    // are .sync.aligned and need every lane
+    auto wwait = [&](uint32_t bar, uint32_t par, bool cluster_scope) -> bool {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
+      const bool r = cluster_scope ? mbar_wait<true>(bar, par, kWaitNs) : mbar_wait(bar, par, kWaitNs);
+      return __all_sync(0xffffffffu, r);
+    };
+    for (int t = 0; t < T; ++t) {
+      if (!wwait(smem_u32(&sm.s_full), (uint32_t)t & 1u, false)) { ok = false; break; }
+      tc_fence_after();
+      float x[kNt];
+      {
+        uint32_t v[32];
+        tmem_ld32(lane_addr + kColS, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(v[k]);
+        tmem_ld32(lane_addr + kColS + 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) x[32 + k] = __uint_as_float(v[k]);
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.s_free));
+      // swap partial scores with the peer CTA
+      if (t > 0 && !wwait(smem_u32(&sm.sent_free), (uint32_t)(t - 1) & 1u, true)) { ok = false; break; }
+#pragma unroll
+      for (int k = 0; k < kNt; k += 4) st_cluster_v4(peer_x + 4 * k, x[k], x[k + 1], x[k + 2], x[k + 3]);
+      mbar_arrive_remote(peer_recv_full);
+      if (!wwait(smem_u32(&sm.recv_full), (uint32_t)t & 1u, true)) { ok = false; break; }
+      const float4* mine = reinterpret_cast<const float4*>(xbuf + h * kXRowFloats);
+#pragma unroll
+      for (int k = 0; k < kNt / 4; ++k) {
+        const float4 o = mine[k];
+        x[4 * k] += o.x;
+        x[4 * k + 1] += o.y;
+        x[4 * k + 2] += o.z;
+        x[4 * k + 3] += o.w;
+      }
+      mbar_arrive_remote(peer_sent_free);
+      // online softmax, log2 domain
+      const int valid = min(kNt, ke - (kb + t * kNt));
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kNt; ++k) {
+        x[k] = (k < valid) ? x[k] * p.scale_log2 : -INFINITY;
+        tmax = fmaxf(tmax, x[k]);
+      }
+      const bool grow = tmax > m_ref + kRescaleLog2;
+      float alpha = 1.f;
+      if (grow) {
+        alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - tmax);
+        m_ref = tmax;
+      }
+      l *= alpha;
+      uint32_t pk[kNt / 2];
+#pragma unroll
+      for (int k = 0; k < kNt; k += 2) {
+        const float p0 = ex2(x[k] - m_ref), p1 = ex2(x[k + 1] - m_ref);
+        l += p0 + p1;
+        pk[k / 2] = pack_bf16x2(p0, p1);
+      }
+      // PV of the previous tile must be done before O is rescaled or P rewritten
+      if (t > 0) {
+        if (!wwait(smem_u32(&sm.pv_done), (uint32_t)(t - 1) & 1u, false)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, grow)) {
+          for (int c = 0; c < 256; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(lane_addr + kColO + c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+            tmem_st32(lane_addr + kColO + c, v);
+          }
+        }
+      }
+      if (valid < kNt) {
+        // ragged last tile: rows past the sequence hold whatever the cache
+        // block holds; zero their value part so 0 * (NaN/Inf) cannot reach O.
+        // Whole 128-byte rows, so the swizzle does not matter.
+        uint4* st = reinterpret_cast<uint4*>(stages + (t % kStages) * kStageBytes);
+        const int n16 = (kNt - valid) * 8;               // uint4 per chunk
+        for (int idx = tid - 64; idx < 4 * n16; idx += 128) {
+          const int c = idx / n16, w = idx % n16;
+          st[(c * kChunkBytes) / 16 + valid * 8 + w] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+      }
+      tmem_st32(lane_addr + kColP, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.p_full));
+    }
+    if (!ok) fail();
+    // epilogue: normalise and write this CTA's half of the output dims
+    const long long urow = (((((long long)r * p.B + b) * p.Lq + i_q) * p.n_split + s_idx) * kHeads + h);
+    float* orow = p.dst_o + urow * kDv + 256 * cta;
+    bool have = ok && T > 0;
+    if (have) {
+      have = wwait(smem_u32(&sm.pv_done), (uint32_t)(T - 1) & 1u, false);
+      if (!have) fail();
+    }
+    tc_fence_after();
+    if (have && l > 0.f) {
+      const float inv = 1.f / l;
+      for (int c = 0; c < 256; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(lane_addr + kColO + c, v);
+        tmem_wait_ld();
+        float4* dst = reinterpret_cast<float4*>(orow + c);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          dst[k] = make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
+                               __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
+      }
+      if (cta == 0) p.dst_lse[urow] = (m_ref + log2f(l)) * 0.69314718055994531f;
+    } else {
+      float4* dst = reinterpret_cast<float4*>(orow);
+      for (int k = 0; k < 64; ++k) dst[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (cta == 0) p.dst_lse[urow] = -INFINITY;
+    }
+  }
+
+  // teardown: the peer no longer touches our shared memory, then free TMEM
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+size_t mla_smem_bytes() { return 1024 + (size_t)kStages * kStageBytes + kXBytes + sizeof(Smem) + 64; }
+
+}  // namespace
+
+bool mla_tc_supported(const AttnArgs& a) {
+  return a.kind == DCP_ATTN_MLA && a.Hq == kHeads && a.Hkv == 1 && a.Dqk == kDqk && a.Dv == kDv &&
+         a.bs == 128 && (long long)a.num_blocks * a.bs < (1LL << 31);
+}
+
+SplitPlan plan_attn_mla_tc(const AttnArgs& a, int sm_count) {
+  return plan_splits(a, sm_count, kNt, 2 * a.Lq);
+}
+
+cudaError_t launch_attn_mla_tc(const AttnArgs& a, const SplitPlan& plan) {
+  CUtensorMap tm_lat, tm_rope;
+  const uint64_t dims[2] = {(uint64_t)kDqk, (uint64_t)a.num_blocks * a.bs};
+  const uint64_t strides[1] = {(uint64_t)kDqk * 2};
+  const uint32_t box_lat[2] = {64, kNt};
+  const uint32_t box_rope[2] = {32, kNt};
+  if (!make_tensor_map_bf16(&tm_lat, a.kv, 2, dims, strides, box_lat, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tensor_map_bf16(&tm_rope, a.kv, 2, dims, strides, box_rope, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  MlaParams p;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.block_tables = a.block_tables;
+  p.seq_lens = a.seq_lens;
+  p.status = a.status;
+  p.B = a.B;
+  p.Lq = a.Lq;
+  p.N = a.N;
+  p.I = a.I;
+  p.max_lb = a.max_lb;
+  p.bs = a.bs;
+  p.num_blocks = a.num_blocks;
+  p.n_split = plan.n_split;
+  p.split_tokens = plan.split_tokens;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  if (plan.n_split > 1) {
+    const size_t rows = (size_t)a.N * a.B * a.Lq * a.Hq;
+    const size_t o_bytes = rows * plan.n_split * a.Dv * sizeof(float);
+    p.dst_o = static_cast<float*>(a.workspace);
+    p.dst_lse = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + ((o_bytes + 255) & ~size_t(255)));
+  } else {
+    p.dst_o = a.partial_out;
+    p.dst_lse = a.lse;
+  }
+  const size_t smem = mla_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(mla_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const long long units = (long long)a.N * a.B * a.Lq * plan.n_split;
+  if (units == 0) return cudaSuccess;
+  mla_attn_kernel<<<(unsigned)(2 * units), kThreads, smem, a.stream>>>(tm_lat, tm_rope, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || plan.n_split <= 1) return e;
+  return launch_split_combine(a, plan);
+}
+
+}  // namespace dcp

@@ -69,15 +69,17 @@ dcp_status_t make_args(const dcp_attn_desc_t* d, int32_t dcp_size, int32_t inter
 }
 
 // The kernel that will run for these arguments, and its split plan.
-enum class Impl { kSimt };
+enum class Impl { kSimt, kMlaTc };
 
 Impl select_impl(const AttnArgs& a) {
-  (void)a;
+  if (mla_tc_supported(a)) return Impl::kMlaTc;
   return Impl::kSimt;
 }
 
 SplitPlan plan_for(const AttnArgs& a, Impl impl, int sm_count) {
   switch (impl) {
+    case Impl::kMlaTc:
+      return plan_attn_mla_tc(a, sm_count);
     case Impl::kSimt:
     default:
       return plan_attn_simt(a, sm_count);
@@ -190,6 +192,8 @@ dcp_status_t dcp_decode_attn(const dcp_attn_desc_t* d, const void* q, const void
   if (!a.status) return DCP_ERR_CUDA;
   a.stream = static_cast<cudaStream_t>(stream);
   switch (impl) {
+    case Impl::kMlaTc:
+      return from_cuda(launch_attn_mla_tc(a, plan));
     case Impl::kSimt:
     default:
       return from_cuda(launch_attn_simt(a, plan));

@@ -58,4 +58,9 @@ cudaError_t launch_split_combine(const AttnArgs& a, const SplitPlan& p);
 cudaError_t launch_attn_simt(const AttnArgs& a, const SplitPlan& p);
 SplitPlan plan_attn_simt(const AttnArgs& a, int sm_count);
 
+// MLA on tcgen05 (Hq 128, Dqk 576, Dv 512, block 128): cluster-pair kernel.
+bool mla_tc_supported(const AttnArgs& a);
+SplitPlan plan_attn_mla_tc(const AttnArgs& a, int sm_count);
+cudaError_t launch_attn_mla_tc(const AttnArgs& a, const SplitPlan& p);
+
 }  // namespace dcp

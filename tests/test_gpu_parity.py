@@ -86,6 +86,8 @@ ATTN_CASES = [
     ("mla_mtp", dict(lengths=("fixed", 2500))),
     ("mla_mtp", dict(lengths=("fixed", 4))),                                # S == Lq
     ("mla_mtp", dict(lengths=("fixed", 300), dcp_size=1)),
+    ("mla_mtp", dict(lengths=("fixed", 40000))),                            # KV splits + combine
+    ("mla_32", dict(batch=3, lengths=("uniform", 1, 700), dcp_size=4, interleave=3)),
 ]
 
 
