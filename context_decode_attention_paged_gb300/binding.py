@@ -44,6 +44,9 @@ _lib.dcp_decode_attn_workspace_size.argtypes = [ctypes.POINTER(DcpAttnDesc), _i3
 _lib.dcp_decode_attn.restype = _i32
 _lib.dcp_decode_attn.argtypes = [ctypes.POINTER(DcpAttnDesc), _vp, _vp, _vp, _vp, _i32, _i32,
                                  _f32, _i32, _vp, _vp, _vp, _sz, _vp]
+_lib.dcp_decode_attn_noalloc.restype = _i32
+_lib.dcp_decode_attn_noalloc.argtypes = [ctypes.POINTER(DcpAttnDesc), _vp, _vp, _vp, _vp, _i32,
+                                         _i32, _f32, _i32, _vp, _vp, _vp]
 _lib.dcp_merge.restype = _i32
 _lib.dcp_merge.argtypes = [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]
 _lib.dcp_get_last_device_status.restype = _i32
@@ -132,6 +135,19 @@ def dcp_decode_attn(kind, q, kv_cache, block_tables, seq_lens, dcp_size, interle
                                 causal_q_len, _ptr(partial_out), _ptr(lse), _ptr(workspace),
                                 workspace.numel() if workspace is not None else 0,
                                 _stream(stream)), "dcp_decode_attn")
+    return partial_out, lse
+
+
+def dcp_decode_attn_noalloc(kind, q, kv_cache, block_tables, seq_lens, dcp_size, interleave,
+                            scale, causal_q_len, head_dim_v, partial_out, lse, stream=None):
+    """dcp_decode_attn without a workspace argument: split scratch comes from the
+    library's built-in array (for callers that may not allocate device memory).
+    Outputs must be passed in; calls overlapping on the GPU share that array."""
+    desc = desc_from_tensors(kind, q, kv_cache, block_tables, head_dim_v)
+    _check(_lib.dcp_decode_attn_noalloc(ctypes.byref(desc), _ptr(q), _ptr(kv_cache),
+                                        _ptr(block_tables), _ptr(seq_lens), dcp_size, interleave,
+                                        float(scale), causal_q_len, _ptr(partial_out), _ptr(lse),
+                                        _stream(stream)), "dcp_decode_attn_noalloc")
     return partial_out, lse
 
 

@@ -156,6 +156,35 @@ DCP_API dcp_status_t dcp_merge(const float* partial_out, const float* lse, int32
                        int32_t batch, int32_t q_len, int32_t num_q_heads, int32_t head_dim_v,
                        void* out, float* out_lse, void* stream);
 
+/* dcp_decode_attn for callers that cannot allocate device memory.
+ * No counterpart in the pages: this is a library convenience, not a step of
+ * the method.  dcp_decode_attn takes caller-allocated scratch when it splits a
+ * shard's keys over several CTAs (small batches with long contexts).  Callers
+ * that may not call cudaMalloc at that point - code inside another runtime's
+ * memory pool, plugins that are handed only their input and output buffers, a
+ * serving loop that forbids allocation on the decode path - use this call
+ * instead: the scratch is a fixed array of DCP_NOALLOC_SCRATCH_BYTES compiled
+ * into the library, held on every GPU that loads the library until exit.
+ * Arguments, results and errors are those of dcp_decode_attn, without the
+ * workspace.  Extra rules:
+ *  - a shape whose dcp_decode_attn_workspace_size exceeds
+ *    DCP_NOALLOC_SCRATCH_BYTES is rejected with DCP_ERR_INVALID_ARG before any
+ *    launch (check that size first to tell this case apart);
+ *  - every call shares the one array, which keeps the last call's contents
+ *    (nothing in it needs to start at zero); calls whose kernels overlap on
+ *    the GPU - on different streams or from different host threads - race on
+ *    it and give wrong results; calls ordered on one stream are safe;
+ *  - the first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ * It calls no allocator (no cudaMalloc/cudaFree) itself.                     */
+#define DCP_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+DCP_API dcp_status_t dcp_decode_attn_noalloc(const dcp_attn_desc_t* d, const void* q,
+                                             const void* kv_cache, const int32_t* block_tables,
+                                             const int32_t* seq_lens, int32_t dcp_size,
+                                             int32_t interleave, float scale,
+                                             int32_t causal_q_len, float* partial_out, float* lse,
+                                             void* stream);
+
 /* Synchronises `stream`, returns the device status word set by earlier kernels
  * (DCP_OK if none) and clears it. */
 DCP_API dcp_status_t dcp_get_last_device_status(void* stream);
