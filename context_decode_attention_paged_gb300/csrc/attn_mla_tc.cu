@@ -47,8 +47,9 @@ constexpr int kStages = 5;
 constexpr uint32_t kChunkBytes = kNt * 128;   // 64 tokens x 64 dims bf16, 128B rows
 constexpr uint32_t kRopeBytes = kNt * 64;     // 64 tokens x 32 dims bf16, 64B rows
 constexpr uint32_t kStageBytes = 4 * kChunkBytes + kRopeBytes;   // 36 KB
-constexpr uint32_t kXRowFloats = 68;          // exchange row: 64 scores + pad (bank spread)
-constexpr uint32_t kXBytes = kHeads * kXRowFloats * 4;
+// Exchange buffer, chunk-major: float4 chunk k of head h at (k * 128 + h) * 16
+// bytes, so one warp's store (or load) of chunk k covers 512 contiguous bytes.
+constexpr uint32_t kXBytes = kHeads * kNt * 4;
 constexpr uint32_t kThreads = 192;
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 // TMEM columns
@@ -122,8 +123,8 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
     mbar_init(smem_u32(&sm.s_free), 128);
     mbar_init(smem_u32(&sm.p_full), 128);
     mbar_init(smem_u32(&sm.pv_done), 1);
-    mbar_init(smem_u32(&sm.recv_full), 128);
-    mbar_init(smem_u32(&sm.sent_free), 128);
+    mbar_init(smem_u32(&sm.recv_full), 1);    // armed with the tile's bytes each round
+    mbar_init(smem_u32(&sm.sent_free), 1);    // one "read done" signal from the peer
     mbar_init(smem_u32(&sm.drain), 1);
     sm.abort = 0;
     fence_mbar_init();
@@ -254,7 +255,7 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
     const int lg = warp & 3;                       // TMEM lane group
     const int h = lg * 32 + lane;                  // query head = TMEM lane
     const uint32_t lane_addr = taddr(tmem, (uint32_t)(lg * 32), 0);
-    const uint32_t my_x = smem_u32(xbuf + h * kXRowFloats);
+    const uint32_t my_x = smem_u32(xbuf + 4 * h);
     const uint32_t peer_x = mapa(my_x, peer);
     const uint32_t peer_recv_full = mapa(smem_u32(&sm.recv_full), peer);
     const uint32_t peer_sent_free = mapa(smem_u32(&sm.sent_free), peer);
@@ -285,21 +286,23 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.s_free));
       // swap partial scores with the peer CTA
-      if (t > 0 && !wwait(smem_u32(&sm.sent_free), (uint32_t)(t - 1) & 1u, true)) { ok = false; break; }
+      if (t > 0 && !wwait(smem_u32(&sm.sent_free), (uint32_t)(t - 1) & 1u, false)) { ok = false; break; }
 #pragma unroll
-      for (int k = 0; k < kNt; k += 4) st_cluster_v4(peer_x + 4 * k, x[k], x[k + 1], x[k + 2], x[k + 3]);
-      mbar_arrive_remote(peer_recv_full);
-      if (!wwait(smem_u32(&sm.recv_full), (uint32_t)t & 1u, true)) { ok = false; break; }
-      const float4* mine = reinterpret_cast<const float4*>(xbuf + h * kXRowFloats);
+      for (int k = 0; k < kNt; k += 4)
+        st_async_v4(peer_x + (k / 4) * (kHeads * 16), x[k], x[k + 1], x[k + 2], x[k + 3], peer_recv_full);
+      if (tid == 64) mbar_arrive_expect_tx(smem_u32(&sm.recv_full), kHeads * kNt * 4);
+      if (!wwait(smem_u32(&sm.recv_full), (uint32_t)t & 1u, false)) { ok = false; break; }
+      const float4* mine = reinterpret_cast<const float4*>(xbuf + 4 * h);
 #pragma unroll
       for (int k = 0; k < kNt / 4; ++k) {
-        const float4 o = mine[k];
+        const float4 o = mine[k * kHeads];
         x[4 * k] += o.x;
         x[4 * k + 1] += o.y;
         x[4 * k + 2] += o.z;
         x[4 * k + 3] += o.w;
       }
-      mbar_arrive_remote(peer_sent_free);
+      named_bar_sync(1, 128);                  // all rows read: the peer may refill
+      if (tid == 64) mbar_arrive_remote_signal(peer_sent_free);
       // online softmax, log2 domain
       const int valid = min(kNt, ke - (kb + t * kNt));
       float tmax = -INFINITY;

@@ -48,6 +48,20 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
                :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
+// Asynchronous 16-byte store into another CTA's shared memory; on arrival it
+// counts 16 bytes of transaction on that CTA's mbarrier `cluster_bar` (both
+// addresses from mapa).  The sender needs no fence.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d,
+                                            uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+               :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar) : "memory");
+}
+
+// Named barrier over `count` threads (multiple of 32); id 0 is __syncthreads.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -73,6 +87,12 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
                :: "r"(cluster_bar) : "memory");
+}
+
+// Arrive on another CTA's barrier without a cluster-scope release (a "done
+// reading" signal that publishes no data).
+__device__ __forceinline__ void mbar_arrive_remote_signal(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" :: "r"(cluster_bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
