@@ -69,10 +69,11 @@ dcp_status_t make_args(const dcp_attn_desc_t* d, int32_t dcp_size, int32_t inter
 }
 
 // The kernel that will run for these arguments, and its split plan.
-enum class Impl { kSimt, kMlaTc };
+enum class Impl { kSimt, kMlaTc, kGqaTc };
 
 Impl select_impl(const AttnArgs& a) {
   if (mla_tc_supported(a)) return Impl::kMlaTc;
+  if (gqa_tc_supported(a)) return Impl::kGqaTc;
   return Impl::kSimt;
 }
 
@@ -80,6 +81,8 @@ SplitPlan plan_for(const AttnArgs& a, Impl impl, int sm_count) {
   switch (impl) {
     case Impl::kMlaTc:
       return plan_attn_mla_tc(a, sm_count);
+    case Impl::kGqaTc:
+      return plan_attn_gqa_tc(a, sm_count);
     case Impl::kSimt:
     default:
       return plan_attn_simt(a, sm_count);
@@ -194,6 +197,8 @@ dcp_status_t dcp_decode_attn(const dcp_attn_desc_t* d, const void* q, const void
   switch (impl) {
     case Impl::kMlaTc:
       return from_cuda(launch_attn_mla_tc(a, plan));
+    case Impl::kGqaTc:
+      return from_cuda(launch_attn_gqa_tc(a, plan));
     case Impl::kSimt:
     default:
       return from_cuda(launch_attn_simt(a, plan));

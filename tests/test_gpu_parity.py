@@ -88,6 +88,13 @@ ATTN_CASES = [
     ("mla_mtp", dict(lengths=("fixed", 300), dcp_size=1)),
     ("mla_mtp", dict(lengths=("fixed", 40000))),                            # KV splits + combine
     ("mla_32", dict(batch=3, lengths=("uniform", 1, 700), dcp_size=4, interleave=3)),
+    # GQA tensor-core kernel: 2 and 4 lane groups of real rows (Lq 4 and 8 x 16 heads)
+    ("qwen_gqa", dict(batch=2, q_len=4, lengths=("uniform", 200, 1500), dcp_size=2)),
+    ("qwen_gqa", dict(batch=1, q_len=8, lengths=("fixed", 3000), dcp_size=2, interleave=64)),
+    # head dims without a tensor-core kernel run on the generic SIMT kernel
+    ("tiny_gqa", dict(head_dim_qk=96, head_dim_v=96, lengths=("fixed", 500))),
+    ("mla_32", dict(batch=2, num_q_heads=16, head_dim_qk=72, head_dim_v=64,
+                    lengths=("uniform", 100, 900), dcp_size=4)),
 ]
 
 
