@@ -43,7 +43,7 @@ using namespace sm100;
 constexpr int kHeads = 128;
 constexpr int kDqk = 576, kDv = 512, kLatent = 512;
 constexpr int kNt = 64;                       // tokens per KV tile (half a 128-token block)
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr uint32_t kChunkBytes = kNt * 128;   // 64 tokens x 64 dims bf16, 128B rows
 constexpr uint32_t kRopeBytes = kNt * 64;     // 64 tokens x 32 dims bf16, 64B rows
 constexpr uint32_t kStageBytes = 4 * kChunkBytes + kRopeBytes;   // 36 KB
@@ -80,6 +80,8 @@ struct Smem {
   uint64_t s_full, s_free, p_full, pv_done, drain;
   uint64_t recv_full[2];   // armed with a tile's bytes; the peer's async stores count them
   uint64_t sent_free[2];   // the peer has read what we stored into its buffer k
+  uint64_t own_full;       // the senders copied this CTA's partial scores to `own`
+  uint64_t own_free;       // the softmax warps have read `own`
   uint32_t tmem_base;
   int abort;
 };
@@ -97,7 +99,8 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = base;                                        // kStages x 36 KB
   float* xbuf = reinterpret_cast<float*>(base + kStages * kStageBytes);   // 2 buffers: peer's scores land here
-  Smem& sm = *reinterpret_cast<Smem*>(base + kStages * kStageBytes + 2 * kXBytes);
+  float* own = xbuf + 2 * (kXBytes / 4);           // this CTA's partial scores (same layout)
+  Smem& sm = *reinterpret_cast<Smem*>(base + kStages * kStageBytes + 3 * kXBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t cta = cluster_ctarank();          // 0 or 1
@@ -126,7 +129,9 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       mbar_init(smem_u32(&sm.kv_empty[k]), 1);
     }
     mbar_init(smem_u32(&sm.s_full), 1);
-    mbar_init(smem_u32(&sm.s_free), 256);     // softmax and sender warpgroups
+    mbar_init(smem_u32(&sm.s_free), 128);     // the sender warpgroup reads S
+    mbar_init(smem_u32(&sm.own_full), 128);
+    mbar_init(smem_u32(&sm.own_free), 128);
     mbar_init(smem_u32(&sm.p_full), 128);
     mbar_init(smem_u32(&sm.pv_done), 1);
     for (int k = 0; k < 2; ++k) {
@@ -235,14 +240,14 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
         mma_commit(smem_u32(&sm.kv_empty[t % kStages]));
         return true;
       };
-      bool ok = true;
-      for (int t = 0; t < T && ok; ++t) {
+      // score tile t+1 is issued as soon as the senders freed S (before tile
+      // t's PV, which waits for the softmax), so QK^T and the score exchange
+      // run one tile ahead of the softmax
+      auto issue_qk = [&](int t) -> bool {
         const int st = t % kStages;
         if (*abort_flag || !mbar_wait(smem_u32(&sm.kv_full[st]), (uint32_t)(t / kStages) & 1u, kWaitNs) ||
-            (t > 0 && !mbar_wait(smem_u32(&sm.s_free), (uint32_t)(t - 1) & 1u, kWaitNs))) {
-          ok = false;
-          break;
-        }
+            (t > 0 && !mbar_wait(smem_u32(&sm.s_free), (uint32_t)(t - 1) & 1u, kWaitNs)))
+          return false;
         tc_fence_after();
         const uint8_t* sb = stages + st * kStageBytes;
 #pragma unroll
@@ -253,9 +258,13 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
           mma_ts(tmem + kColS, tmem + kColQ + 8 * k, bdesc, id_qk, k > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(&sm.s_full));
-        if (t > 0) ok = issue_pv(t - 1);
+        return true;
+      };
+      bool ok = issue_qk(0);
+      for (int t = 0; t < T && ok; ++t) {
+        if (t + 1 < T && !(ok = issue_qk(t + 1))) break;
+        ok = issue_pv(t);
       }
-      if (ok) ok = issue_pv(T - 1);
       if (!ok) fail();
       // drain: arrives when every MMA issued above has completed
       mma_commit(smem_u32(&sm.drain));
@@ -279,36 +288,29 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       return __all_sync(0xffffffffu, r);
     };
     for (int t = 0; t < T; ++t) {
-      if (!wwait(smem_u32(&sm.s_full), (uint32_t)t & 1u, false)) { ok = false; break; }
-      tc_fence_after();
-      float x[kNt];
-      {
-        uint32_t v[32];
-        tmem_ld32(lane_addr + kColS, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(v[k]);
-        tmem_ld32(lane_addr + kColS + 32, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 32; ++k) x[32 + k] = __uint_as_float(v[k]);
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.s_free));
-      // the sender warpgroup has pushed our partial scores of tile t to the
-      // peer; wait for the peer's partial of tile t in exchange buffer t & 1
+      // both partial score tiles come from shared memory: ours copied there
+      // by the sender warpgroup, the peer's delivered by its async stores
       const int xb = t & 1;
       if (tid == 128) mbar_arrive_expect_tx(smem_u32(&sm.recv_full[xb]), kXBytes);
-      if (!wwait(smem_u32(&sm.recv_full[xb]), (uint32_t)(t >> 1) & 1u, false)) { ok = false; break; }
-      const float4* mine = reinterpret_cast<const float4*>(xbuf + xb * (kXBytes / 4) + 4 * h);
-#pragma unroll
-      for (int k = 0; k < kNt / 4; ++k) {
-        const float4 o = mine[k * kHeads];
-        x[4 * k] += o.x;
-        x[4 * k + 1] += o.y;
-        x[4 * k + 2] += o.z;
-        x[4 * k + 3] += o.w;
+      if (!wwait(smem_u32(&sm.own_full), (uint32_t)t & 1u, false) ||
+          !wwait(smem_u32(&sm.recv_full[xb]), (uint32_t)(t >> 1) & 1u, false)) {
+        ok = false;
+        break;
       }
+      float x[kNt];
+      {
+        const float4* mine = reinterpret_cast<const float4*>(own + 4 * h);
+        const float4* theirs = reinterpret_cast<const float4*>(xbuf + xb * (kXBytes / 4) + 4 * h);
+#pragma unroll
+        for (int k = 0; k < kNt / 4; ++k) {
+          const float4 a = mine[k * kHeads], o = theirs[k * kHeads];
+          x[4 * k] = a.x + o.x;
+          x[4 * k + 1] = a.y + o.y;
+          x[4 * k + 2] = a.z + o.z;
+          x[4 * k + 3] = a.w + o.w;
+        }
+      }
+      mbar_arrive(smem_u32(&sm.own_free));
       named_bar_sync(1, 128);                  // all rows read: the peer may refill buffer xb
       if (tid == 128) mbar_arrive_remote_signal(peer_sent_free + 8 * xb);
       // online softmax, log2 domain
@@ -434,6 +436,21 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       for (int k = 0; k < 8; ++k)
         st_async_v4(dst + (8 + k) * (kHeads * 16), __uint_as_float(v1[4 * k]), __uint_as_float(v1[4 * k + 1]),
                     __uint_as_float(v1[4 * k + 2]), __uint_as_float(v1[4 * k + 3]), bar);
+      // our own copy for the softmax warpgroup (same chunk-major layout)
+      if (t >= 1 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.own_free), (uint32_t)(t - 1) & 1u, kWaitNs))) {
+        ok = false;
+        break;
+      }
+      float4* mine = reinterpret_cast<float4*>(own + 4 * h);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        mine[k * kHeads] = make_float4(__uint_as_float(v0[4 * k]), __uint_as_float(v0[4 * k + 1]),
+                                       __uint_as_float(v0[4 * k + 2]), __uint_as_float(v0[4 * k + 3]));
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        mine[(8 + k) * kHeads] = make_float4(__uint_as_float(v1[4 * k]), __uint_as_float(v1[4 * k + 1]),
+                                             __uint_as_float(v1[4 * k + 2]), __uint_as_float(v1[4 * k + 3]));
+      mbar_arrive(smem_u32(&sm.own_full));
     }
     if (!ok) fail();
   }
@@ -448,7 +465,7 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
   }
 }
 
-size_t mla_smem_bytes() { return 1024 + (size_t)kStages * kStageBytes + 2 * kXBytes + sizeof(Smem) + 64; }
+size_t mla_smem_bytes() { return 1024 + (size_t)kStages * kStageBytes + 3 * kXBytes + sizeof(Smem) + 64; }
 
 }  // namespace
 
