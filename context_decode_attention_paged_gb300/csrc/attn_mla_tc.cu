@@ -43,7 +43,7 @@ using namespace sm100;
 constexpr int kHeads = 128;
 constexpr int kDqk = 576, kDv = 512, kLatent = 512;
 constexpr int kNt = 64;                       // tokens per KV tile (half a 128-token block)
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr uint32_t kChunkBytes = kNt * 128;   // 64 tokens x 64 dims bf16, 128B rows
 constexpr uint32_t kRopeBytes = kNt * 64;     // 64 tokens x 32 dims bf16, 64B rows
 constexpr uint32_t kStageBytes = 4 * kChunkBytes + kRopeBytes;   // 36 KB
@@ -53,7 +53,7 @@ constexpr uint32_t kXBytes = kHeads * kNt * 4;
 constexpr uint32_t kThreads = 384;             // 3 warpgroups
 // Register split (setmaxnreg) against the 384 x 168 registers of the launch:
 // control warpgroup and score senders give registers up, softmax takes them.
-constexpr int kLaunchRegs = 168, kCtrlRegs = 96, kSendRegs = 112, kSoftRegs = 200;
+constexpr int kLaunchRegs = 168, kCtrlRegs = 96, kSendRegs = 104, kSoftRegs = 232;
 static_assert(128 * (kCtrlRegs + kSendRegs + kSoftRegs) <= 384 * kLaunchRegs, "register split exceeds the launch");
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 // TMEM columns
@@ -77,11 +77,9 @@ struct MlaParams {
 struct Smem {
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
-  uint64_t s_full, s_free, p_full, pv_done, drain;
+  uint64_t s_full, s_free, p_full, pv_done, drain, drain_qk;
   uint64_t recv_full[2];   // armed with a tile's bytes; the peer's async stores count them
   uint64_t sent_free[2];   // the peer has read what we stored into its buffer k
-  uint64_t own_full;       // the senders copied this CTA's partial scores to `own`
-  uint64_t own_free;       // the softmax warps have read `own`
   uint32_t tmem_base;
   int abort;
 };
@@ -99,8 +97,7 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = base;                                        // kStages x 36 KB
   float* xbuf = reinterpret_cast<float*>(base + kStages * kStageBytes);   // 2 buffers: peer's scores land here
-  float* own = xbuf + 2 * (kXBytes / 4);           // this CTA's partial scores (same layout)
-  Smem& sm = *reinterpret_cast<Smem*>(base + kStages * kStageBytes + 3 * kXBytes);
+  Smem& sm = *reinterpret_cast<Smem*>(base + kStages * kStageBytes + 2 * kXBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t cta = cluster_ctarank();          // 0 or 1
@@ -129,9 +126,7 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       mbar_init(smem_u32(&sm.kv_empty[k]), 1);
     }
     mbar_init(smem_u32(&sm.s_full), 1);
-    mbar_init(smem_u32(&sm.s_free), 128);     // the sender warpgroup reads S
-    mbar_init(smem_u32(&sm.own_full), 128);
-    mbar_init(smem_u32(&sm.own_free), 128);
+    mbar_init(smem_u32(&sm.s_free), 256);     // softmax and sender warpgroups
     mbar_init(smem_u32(&sm.p_full), 128);
     mbar_init(smem_u32(&sm.pv_done), 1);
     for (int k = 0; k < 2; ++k) {
@@ -139,6 +134,7 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       mbar_init(smem_u32(&sm.sent_free[k]), 1);
     }
     mbar_init(smem_u32(&sm.drain), 1);
+    mbar_init(smem_u32(&sm.drain_qk), 1);
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -223,12 +219,17 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+    // ---------------- PV issuer (and TMEM owner) ----------------
+    // Score and PV MMAs come from two threads, so the score tile of t+1 (and
+    // its exchange) never waits behind tile t's PV, which waits for the softmax.
     if (lane == 0 && T > 0) {
-      const uint32_t id_qk = idesc_bf16(128, kNt, false);
       const uint32_t id_pv = idesc_bf16(128, 256, true);
-      auto issue_pv = [&](int t) -> bool {
-        if (*abort_flag || !mbar_wait(smem_u32(&sm.p_full), (uint32_t)t & 1u, kWaitNs)) return false;
+      bool ok = true;
+      for (int t = 0; t < T; ++t) {
+        if (*abort_flag || !mbar_wait(smem_u32(&sm.p_full), (uint32_t)t & 1u, kWaitNs)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint8_t* st = stages + (t % kStages) * kStageBytes;
 #pragma unroll
@@ -237,17 +238,25 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
           mma_ts(tmem + kColO, tmem + kColP + 8 * k, bdesc, id_pv, (t > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(smem_u32(&sm.pv_done));
+        // the score MMAs of tile t completed before the softmax produced P_t
         mma_commit(smem_u32(&sm.kv_empty[t % kStages]));
-        return true;
-      };
-      // score tile t+1 is issued as soon as the senders freed S (before tile
-      // t's PV, which waits for the softmax), so QK^T and the score exchange
-      // run one tile ahead of the softmax
-      auto issue_qk = [&](int t) -> bool {
+      }
+      if (!ok) fail();
+      mma_commit(smem_u32(&sm.drain));
+      if (!mbar_wait(smem_u32(&sm.drain), 0, kWaitNs)) fail();
+    }
+  } else if (warp == 2) {
+    // ---------------- score (QK^T) issuer ----------------
+    if (lane == 0 && T > 0) {
+      const uint32_t id_qk = idesc_bf16(128, kNt, false);
+      bool ok = true;
+      for (int t = 0; t < T; ++t) {
         const int st = t % kStages;
         if (*abort_flag || !mbar_wait(smem_u32(&sm.kv_full[st]), (uint32_t)(t / kStages) & 1u, kWaitNs) ||
-            (t > 0 && !mbar_wait(smem_u32(&sm.s_free), (uint32_t)(t - 1) & 1u, kWaitNs)))
-          return false;
+            (t > 0 && !mbar_wait(smem_u32(&sm.s_free), (uint32_t)(t - 1) & 1u, kWaitNs))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint8_t* sb = stages + st * kStageBytes;
 #pragma unroll
@@ -258,17 +267,10 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
           mma_ts(tmem + kColS, tmem + kColQ + 8 * k, bdesc, id_qk, k > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(&sm.s_full));
-        return true;
-      };
-      bool ok = issue_qk(0);
-      for (int t = 0; t < T && ok; ++t) {
-        if (t + 1 < T && !(ok = issue_qk(t + 1))) break;
-        ok = issue_pv(t);
       }
       if (!ok) fail();
-      // drain: arrives when every MMA issued above has completed
-      mma_commit(smem_u32(&sm.drain));
-      if (!mbar_wait(smem_u32(&sm.drain), 0, kWaitNs)) fail();
+      mma_commit(smem_u32(&sm.drain_qk));
+      if (!mbar_wait(smem_u32(&sm.drain_qk), 0, kWaitNs)) fail();
     }
   }
   } else if (warp < 8) {
@@ -287,32 +289,47 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       const bool r = cluster_scope ? mbar_wait<true>(bar, par, kWaitNs) : mbar_wait(bar, par, kWaitNs);
       return __all_sync(0xffffffffu, r);
     };
-    for (int t = 0; t < T; ++t) {
-      // both partial score tiles come from shared memory: ours copied there
-      // by the sender warpgroup, the peer's delivered by its async stores
+    // One-tile lookahead: tile t+1's partial scores are read out of TMEM (and
+    // S released to the score MMA) before tile t's softmax is computed.
+    float nx[kNt];
+    auto load_scores = [&](int t) -> bool {
+      if (!wwait(smem_u32(&sm.s_full), (uint32_t)t & 1u, false)) return false;
+      tc_fence_after();
+      uint32_t v0[32], v1[32];
+      tmem_ld32(lane_addr + kColS, v0);
+      tmem_ld32(lane_addr + kColS + 32, v1);
+      tmem_wait_ld();
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        nx[k] = __uint_as_float(v0[k]);
+        nx[32 + k] = __uint_as_float(v1[k]);
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.s_free));
+      return true;
+    };
+    if (T > 0 && !load_scores(0)) ok = false;
+    for (int t = 0; t < T && ok; ++t) {
+      float x[kNt];
+#pragma unroll
+      for (int k = 0; k < kNt; ++k) x[k] = nx[k];
+      // the sender warpgroup has pushed our partial scores of tile t to the
+      // peer; wait for the peer's partial of tile t in exchange buffer t & 1
       const int xb = t & 1;
       if (tid == 128) mbar_arrive_expect_tx(smem_u32(&sm.recv_full[xb]), kXBytes);
-      if (!wwait(smem_u32(&sm.own_full), (uint32_t)t & 1u, false) ||
-          !wwait(smem_u32(&sm.recv_full[xb]), (uint32_t)(t >> 1) & 1u, false)) {
-        ok = false;
-        break;
-      }
-      float x[kNt];
-      {
-        const float4* mine = reinterpret_cast<const float4*>(own + 4 * h);
-        const float4* theirs = reinterpret_cast<const float4*>(xbuf + xb * (kXBytes / 4) + 4 * h);
+      if (!wwait(smem_u32(&sm.recv_full[xb]), (uint32_t)(t >> 1) & 1u, false)) { ok = false; break; }
+      const float4* mine = reinterpret_cast<const float4*>(xbuf + xb * (kXBytes / 4) + 4 * h);
 #pragma unroll
-        for (int k = 0; k < kNt / 4; ++k) {
-          const float4 a = mine[k * kHeads], o = theirs[k * kHeads];
-          x[4 * k] = a.x + o.x;
-          x[4 * k + 1] = a.y + o.y;
-          x[4 * k + 2] = a.z + o.z;
-          x[4 * k + 3] = a.w + o.w;
-        }
+      for (int k = 0; k < kNt / 4; ++k) {
+        const float4 o = mine[k * kHeads];
+        x[4 * k] += o.x;
+        x[4 * k + 1] += o.y;
+        x[4 * k + 2] += o.z;
+        x[4 * k + 3] += o.w;
       }
-      mbar_arrive(smem_u32(&sm.own_free));
       named_bar_sync(1, 128);                  // all rows read: the peer may refill buffer xb
       if (tid == 128) mbar_arrive_remote_signal(peer_sent_free + 8 * xb);
+      if (t + 1 < T && !load_scores(t + 1)) { ok = false; break; }
       // online softmax, log2 domain
       const int valid = min(kNt, ke - (kb + t * kNt));
       float tmax = -INFINITY;
@@ -436,21 +453,6 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       for (int k = 0; k < 8; ++k)
         st_async_v4(dst + (8 + k) * (kHeads * 16), __uint_as_float(v1[4 * k]), __uint_as_float(v1[4 * k + 1]),
                     __uint_as_float(v1[4 * k + 2]), __uint_as_float(v1[4 * k + 3]), bar);
-      // our own copy for the softmax warpgroup (same chunk-major layout)
-      if (t >= 1 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.own_free), (uint32_t)(t - 1) & 1u, kWaitNs))) {
-        ok = false;
-        break;
-      }
-      float4* mine = reinterpret_cast<float4*>(own + 4 * h);
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        mine[k * kHeads] = make_float4(__uint_as_float(v0[4 * k]), __uint_as_float(v0[4 * k + 1]),
-                                       __uint_as_float(v0[4 * k + 2]), __uint_as_float(v0[4 * k + 3]));
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        mine[(8 + k) * kHeads] = make_float4(__uint_as_float(v1[4 * k]), __uint_as_float(v1[4 * k + 1]),
-                                             __uint_as_float(v1[4 * k + 2]), __uint_as_float(v1[4 * k + 3]));
-      mbar_arrive(smem_u32(&sm.own_full));
     }
     if (!ok) fail();
   }
@@ -465,7 +467,7 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
   }
 }
 
-size_t mla_smem_bytes() { return 1024 + (size_t)kStages * kStageBytes + 3 * kXBytes + sizeof(Smem) + 64; }
+size_t mla_smem_bytes() { return 1024 + (size_t)kStages * kStageBytes + 2 * kXBytes + sizeof(Smem) + 64; }
 
 }  // namespace
 
