@@ -50,12 +50,12 @@ constexpr uint32_t kStageBytes = 4 * kChunkBytes + kRopeBytes;   // 36 KB
 // Exchange buffer, chunk-major: float4 chunk k of head h at (k * 128 + h) * 16
 // bytes, so one warp's store (or load) of chunk k covers 512 contiguous bytes.
 constexpr uint32_t kXBytes = kHeads * kNt * 4;
-constexpr uint32_t kThreads = 512;             // 4 warpgroups
+constexpr uint32_t kThreads = 640;             // 5 warpgroups
 // Register split (setmaxnreg) against the 384 x 168 registers of the launch:
 // control warpgroup and score senders give registers up, softmax takes them.
-constexpr int kLaunchRegs = 128, kCtrlRegs = 80, kSendRegs = 80, kSoftRegs = 160;
-constexpr int kSplitRegs = 128 * kCtrlRegs + 256 * kSoftRegs + 128 * kSendRegs;   // 61,440
-static_assert(kSplitRegs <= 512 * kLaunchRegs, "register split exceeds the launch");
+constexpr int kLaunchRegs = 96, kCtrlRegs = 48, kSendRegs = 80, kSoftRegs = 136;
+constexpr int kSplitRegs = 128 * kCtrlRegs + 256 * kSoftRegs + 256 * kSendRegs;   // 61,440
+static_assert(kSplitRegs <= 640 * kLaunchRegs, "register split exceeds the launch");
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 // TMEM columns
 constexpr uint32_t kColQ = 0;      // 144 cols: 128 rows x 288 bf16
@@ -434,18 +434,22 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       if (cta == 0 && w == 0) p.dst_lse[urow] = -INFINITY;
     }
   } else {
-    // ---------------- score senders (warps 8..11), give registers up ----------------
+    // ---------------- score senders (warps 12..19), give registers up ----------------
     // Each tile's partial scores go to the peer as 16-byte async stores that
-    // count bytes on the peer's barrier; a dedicated warpgroup does it so the
-    // softmax warps never stall on the DSMEM link.
+    // count bytes on the peer's barrier.  Two warpgroups alternate tiles
+    // (warpgroup k: tiles t = k mod 2, exchange buffer k): a sender thread is
+    // held up while the DSMEM link drains its stores, and the other warpgroup
+    // meanwhile reads the next score tile out of TMEM, so S is released to the
+    // score MMA without waiting for the link.
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kSendRegs));
     const int lg = warp & 3;
     const int h = lg * 32 + lane;
     const uint32_t lane_addr = taddr(tmem, (uint32_t)(lg * 32), 0);
     const uint32_t peer_x = mapa(smem_u32(xbuf + 4 * h), peer);
     const uint32_t peer_recv_full = mapa(smem_u32(&sm.recv_full[0]), peer);
+    const int ks = (warp - 12) >> 2;
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
+    for (int t = ks; t < T; t += 2) {
       if (__any_sync(0xffffffffu, *abort_flag != 0) ||
           !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full), (uint32_t)t & 1u, kWaitNs))) {
         ok = false;
