@@ -79,6 +79,7 @@ struct Smem {
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full, s_free, p_full, pv_done, drain, drain_qk;
+  uint64_t s_full_s[2];    // score tile t ready, for sender warpgroup t & 1 (one phase per own tile)
   uint64_t recv_full[2];   // armed with a tile's bytes; the peer's async stores count them
   uint64_t sent_free[2];   // the peer has read what we stored into its buffer k
   uint64_t xchg[2];        // both softmax warpgroups posted their partial max (count 256)
@@ -143,6 +144,8 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
     }
     mbar_init(smem_u32(&sm.drain), 1);
     mbar_init(smem_u32(&sm.drain_qk), 1);
+    mbar_init(smem_u32(&sm.s_full_s[0]), 1);
+    mbar_init(smem_u32(&sm.s_full_s[1]), 1);
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -275,6 +278,7 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
           mma_ts(tmem + kColS, tmem + kColQ + 8 * k, bdesc, id_qk, k > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(&sm.s_full));
+        mma_commit(smem_u32(&sm.s_full_s[t & 1]));
       }
       if (!ok) fail();
       mma_commit(smem_u32(&sm.drain_qk));
@@ -451,7 +455,7 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
     bool ok = true;
     for (int t = ks; t < T; t += 2) {
       if (__any_sync(0xffffffffu, *abort_flag != 0) ||
-          !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full), (uint32_t)t & 1u, kWaitNs))) {
+          !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full_s[ks]), (uint32_t)(t >> 1) & 1u, kWaitNs))) {
         ok = false;
         break;
       }
