@@ -57,11 +57,12 @@ constexpr uint32_t kStageBytes = 4 * kChunkBytes + kRopeBytes;   // 36 KB
 // bit-identical; the score error is at most |s_partial| * 2^-17.
 constexpr int kXChunks = 12;
 constexpr uint32_t kXBytes = kHeads * kXChunks * 16;
-constexpr uint32_t kThreads = 384;             // 3 warpgroups
+constexpr uint32_t kThreads = 512;             // 4 warpgroups
 // Register split (setmaxnreg) against the 384 x 168 registers of the launch:
 // control warpgroup and score senders give registers up, softmax takes them.
-constexpr int kLaunchRegs = 168, kCtrlRegs = 96, kSendRegs = 104, kSoftRegs = 232;
-static_assert(128 * (kCtrlRegs + kSendRegs + kSoftRegs) <= 384 * kLaunchRegs, "register split exceeds the launch");
+constexpr int kLaunchRegs = 128, kCtrlRegs = 80, kSendRegs = 80, kSoftRegs = 160;
+constexpr int kSplitRegs = 128 * kCtrlRegs + 256 * kSoftRegs + 128 * kSendRegs;   // 61,440
+static_assert(kSplitRegs <= 512 * kLaunchRegs, "register split exceeds the launch");
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 // TMEM columns
 constexpr uint32_t kColQ = 0;      // 144 cols: 128 rows x 288 bf16
@@ -87,8 +88,12 @@ struct Smem {
   uint64_t s_full, s_free, p_full, pv_done, drain, drain_qk;
   uint64_t recv_full[2];   // armed with a tile's bytes; the peer's async stores count them
   uint64_t sent_free[2];   // the peer has read what we stored into its buffer k
+  uint64_t xchg[2];        // both softmax warpgroups posted their partial max (count 256)
+  uint64_t fin;            // both softmax warpgroups posted their row sums (count 256)
   uint32_t tmem_base;
   int abort;
+  float rmax[2][2][kHeads];   // [tile parity][warpgroup][head] partial row max
+  float rsum[2][kHeads];      // [warpgroup][head] row sums, combined at the end
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -151,8 +156,11 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       mbar_init(smem_u32(&sm.kv_empty[k]), 1);
     }
     mbar_init(smem_u32(&sm.s_full), 1);
-    mbar_init(smem_u32(&sm.s_free), 256);     // softmax and sender warpgroups
-    mbar_init(smem_u32(&sm.p_full), 128);
+    mbar_init(smem_u32(&sm.s_free), 384);     // both softmax warpgroups and the senders
+    mbar_init(smem_u32(&sm.p_full), 256);
+    mbar_init(smem_u32(&sm.xchg[0]), 256);
+    mbar_init(smem_u32(&sm.xchg[1]), 256);
+    mbar_init(smem_u32(&sm.fin), 256);
     mbar_init(smem_u32(&sm.pv_done), 1);
     for (int k = 0; k < 2; ++k) {
       mbar_init(smem_u32(&sm.recv_full[k]), 1);
@@ -169,13 +177,13 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
   const uint32_t tmem = sm.tmem_base;
 
   // query slice of this CTA -> TMEM (row = head = TMEM lane, bf16 pairs per column)
-  if (warp >= 4 && warp < 8) {       // the softmax warpgroup stages the query
+  if (warp >= 4 && warp < 12) {      // the softmax warpgroups stage the query
     const int h = (warp & 3) * 32 + lane;
     const uint4* qrow = reinterpret_cast<const uint4*>(
         p.q + (((long long)b * p.Lq + i_q) * kHeads + h) * kDqk);
     const uint32_t lane_addr = taddr(tmem, (uint32_t)((warp & 3) * 32), 0);
-#pragma unroll
-    for (int c = 0; c < 9; ++c) {          // 9 x 16 columns = 288 dims
+    const int wq = (warp - 4) >> 2;
+    for (int c = 5 * wq; c < (wq ? 9 : 5); ++c) {   // 9 x 16 columns = 288 dims, split 5 / 4
       uint32_t v[16];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -298,142 +306,155 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       if (!mbar_wait(smem_u32(&sm.drain_qk), 0, kWaitNs)) fail();
     }
   }
-  } else if (warp < 8) {
-    // ---------------- softmax / epilogue (warps 4..7), takes registers ----------------
+  } else if (warp < 12) {
+    // ---------------- softmax / epilogue (warps 4..11), take registers ----------------
+    // Two warpgroups split every tile's 64 tokens (warpgroup w: tokens
+    // [32w, +32)) and this CTA's 256 output columns (w: [128w, +128)); they
+    // combine partial row maxima once per tile and row sums at the end.
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(kSoftRegs));
+    const int w = (warp - 4) >> 2;
     const int lg = warp & 3;                       // TMEM lane group
     const int h = lg * 32 + lane;                  // query head = TMEM lane
+    const int mt = tid - 128;                      // 0..255 among the softmax threads
     const uint32_t lane_addr = taddr(tmem, (uint32_t)(lg * 32), 0);
     const uint32_t peer_sent_free = mapa(smem_u32(&sm.sent_free[0]), peer);
-    float m_ref = -INFINITY, l = 0.f;
+    float m_ref = -INFINITY, l = 0.f;              // l over this warpgroup's tokens
     bool ok = true;
     // waits and the abort flag are made warp-uniform: the tcgen05 ld/st below
     // are .sync.aligned and need every lane
-    auto wwait = [&](uint32_t bar, uint32_t par, bool cluster_scope) -> bool {
+    auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
-      const bool r = cluster_scope ? mbar_wait<true>(bar, par, kWaitNs) : mbar_wait(bar, par, kWaitNs);
-      return __all_sync(0xffffffffu, r);
+      return __all_sync(0xffffffffu, mbar_wait(bar, par, kWaitNs));
     };
     // One-tile lookahead: tile t+1's partial scores are read out of TMEM (and
     // S released to the score MMA) before tile t's softmax is computed.
-    float nx[kNt];
+    float nx[32];
     auto load_scores = [&](int t) -> bool {
-      if (!wwait(smem_u32(&sm.s_full), (uint32_t)t & 1u, false)) return false;
+      if (!wwait(smem_u32(&sm.s_full), (uint32_t)t & 1u)) return false;
       tc_fence_after();
-      uint32_t v0[32], v1[32];
-      tmem_ld32(lane_addr + kColS, v0);
-      tmem_ld32(lane_addr + kColS + 32, v1);
+      uint32_t v[32];
+      tmem_ld32(lane_addr + kColS + 32 * w, v);
       tmem_wait_ld();
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        nx[k] = __uint_as_float(v0[k]);
-        nx[32 + k] = __uint_as_float(v1[k]);
-      }
+      for (int k = 0; k < 32; ++k) nx[k] = __uint_as_float(v[k]);
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.s_free));
       return true;
     };
     if (T > 0 && !load_scores(0)) ok = false;
     for (int t = 0; t < T && ok; ++t) {
-      float x[kNt];
+      float x[32];
 #pragma unroll
-      for (int k = 0; k < kNt; ++k) x[k] = nx[k];
+      for (int k = 0; k < 32; ++k) x[k] = nx[k];
       // the sender warpgroup has pushed our partial scores of tile t to the
-      // peer; wait for the peer's partial of tile t in exchange buffer t & 1
+      // peer; the peer's partial of tile t arrives in exchange buffer t & 1
       const int xb = t & 1;
-      if (tid == 128) mbar_arrive_expect_tx(smem_u32(&sm.recv_full[xb]), kXBytes);
-      if (!wwait(smem_u32(&sm.recv_full[xb]), (uint32_t)(t >> 1) & 1u, false)) { ok = false; break; }
+      if (mt == 0) mbar_arrive_expect_tx(smem_u32(&sm.recv_full[xb]), kXBytes);
+      if (!wwait(smem_u32(&sm.recv_full[xb]), (uint32_t)(t >> 1) & 1u)) { ok = false; break; }
       {
         const uint4* theirs = reinterpret_cast<const uint4*>(xbuf + xb * (kXBytes / 4)) + h;
-        uint32_t wd[48];
+        uint32_t wd[24];
 #pragma unroll
-        for (int k = 0; k < kXChunks; ++k) {
-          const uint4 q4 = theirs[k * kHeads];
+        for (int k = 0; k < 6; ++k) {
+          const uint4 q4 = theirs[(6 * w + k) * kHeads];
           wd[4 * k] = q4.x;
           wd[4 * k + 1] = q4.y;
           wd[4 * k + 2] = q4.z;
           wd[4 * k + 3] = q4.w;
         }
 #pragma unroll
-        for (int g = 0; g < 16; ++g) {
+        for (int g = 0; g < 8; ++g) {
           float o[4];
           unpack24(wd[3 * g], wd[3 * g + 1], wd[3 * g + 2], o);
 #pragma unroll
           for (int e = 0; e < 4; ++e) x[4 * g + e] = widen24(round24(x[4 * g + e])) + o[e];
         }
       }
-      named_bar_sync(1, 128);                  // all rows read: the peer may refill buffer xb
-      if (tid == 128) mbar_arrive_remote_signal(peer_sent_free + 8 * xb);
-      if (t + 1 < T && !load_scores(t + 1)) { ok = false; break; }
-      // online softmax, log2 domain
-      const int valid = min(kNt, ke - (kb + t * kNt));
-      float tmax = -INFINITY;
+      // online softmax, log2 domain; tree reductions keep dependency chains short
+      const int valid = min(kNt, ke - (kb + t * kNt)) - 32 * w;   // may be <= 0
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int k = 0; k < kNt; ++k) {
+      for (int k = 0; k < 32; ++k) {
         x[k] = (k < valid) ? x[k] * p.scale_log2 : -INFINITY;
-        tmax = fmaxf(tmax, x[k]);
+        m4[k & 3] = fmaxf(m4[k & 3], x[k]);
       }
+      const float pmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      // post the partial max; the barrier also tells us both warpgroups have
+      // read exchange buffer xb, so the peer may refill it
+      sm.rmax[xb][w][h] = pmax;
+      mbar_arrive(smem_u32(&sm.xchg[xb]));
+      if (!wwait(smem_u32(&sm.xchg[xb]), (uint32_t)(t >> 1) & 1u)) { ok = false; break; }
+      if (mt == 0) mbar_arrive_remote_signal(peer_sent_free + 8 * xb);
+      const float tmax = fmaxf(pmax, sm.rmax[xb][w ^ 1][h]);
+      if (t + 1 < T && !load_scores(t + 1)) { ok = false; break; }
       const bool grow = tmax > m_ref + kRescaleLog2;
       float alpha = 1.f;
       if (grow) {
         alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - tmax);
         m_ref = tmax;
       }
-      l *= alpha;
-      uint32_t pk[kNt / 2];
+      uint32_t pk[16];
+      float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int k = 0; k < kNt; k += 2) {
-        const float p0 = ex2(x[k] - m_ref), p1 = ex2(x[k + 1] - m_ref);
-        l += p0 + p1;
+      for (int k = 0; k < 32; k += 2) {
+        const float p0 = (k < valid) ? ex2(x[k] - m_ref) : 0.f;
+        const float p1 = (k + 1 < valid) ? ex2(x[k + 1] - m_ref) : 0.f;
+        l4[(k >> 1) & 3] += p0 + p1;
         pk[k / 2] = pack_bf16x2(p0, p1);
       }
+      l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
       // PV of the previous tile must be done before O is rescaled or P rewritten
       if (t > 0) {
-        if (!wwait(smem_u32(&sm.pv_done), (uint32_t)(t - 1) & 1u, false)) { ok = false; break; }
+        if (!wwait(smem_u32(&sm.pv_done), (uint32_t)(t - 1) & 1u)) { ok = false; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, grow)) {
-          for (int c = 0; c < 256; c += 32) {
+          for (int c = 0; c < 128; c += 32) {
             uint32_t v[32];
-            tmem_ld32(lane_addr + kColO + c, v);
+            tmem_ld32(lane_addr + kColO + 128 * w + c, v);
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-            tmem_st32(lane_addr + kColO + c, v);
+            tmem_st32(lane_addr + kColO + 128 * w + c, v);
           }
         }
       }
-      if (valid < kNt) {
+      const int tv = min(kNt, ke - (kb + t * kNt));
+      if (tv < kNt) {
         // ragged last tile: rows past the sequence hold whatever the cache
         // block holds; zero their value part so 0 * (NaN/Inf) cannot reach O.
         // Whole 128-byte rows, so the swizzle does not matter.
         uint4* st = reinterpret_cast<uint4*>(stages + (t % kStages) * kStageBytes);
-        const int n16 = (kNt - valid) * 8;               // uint4 per chunk
-        for (int idx = tid - 128; idx < 4 * n16; idx += 128) {
-          const int c = idx / n16, w = idx % n16;
-          st[(c * kChunkBytes) / 16 + valid * 8 + w] = make_uint4(0u, 0u, 0u, 0u);
+        const int n16 = (kNt - tv) * 8;                  // uint4 per chunk
+        for (int idx = mt; idx < 4 * n16; idx += 256) {
+          const int c = idx / n16, q = idx % n16;
+          st[(c * kChunkBytes) / 16 + tv * 8 + q] = make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
       }
-      tmem_st32(lane_addr + kColP, pk);
+      tmem_st16(lane_addr + kColP + 16 * w, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.p_full));
     }
     if (!ok) fail();
-    // epilogue: normalise and write this CTA's half of the output dims
-    const long long urow = (((((long long)r * p.B + b) * p.Lq + i_q) * p.n_split + s_idx) * kHeads + h);
-    float* orow = p.dst_o + urow * kDv + 256 * cta;
-    bool have = ok && T > 0;
+    // epilogue: combine the warpgroups' row sums, normalise, write columns
+    // [128w, +128) of this CTA's half of the output dims
+    sm.rsum[w][h] = l;
+    mbar_arrive(smem_u32(&sm.fin));
+    bool have = ok && T > 0 && wwait(smem_u32(&sm.fin), 0u);
     if (have) {
-      have = wwait(smem_u32(&sm.pv_done), (uint32_t)(T - 1) & 1u, false);
+      have = wwait(smem_u32(&sm.pv_done), (uint32_t)(T - 1) & 1u);
       if (!have) fail();
     }
     tc_fence_after();
-    if (have && l > 0.f) {
-      const float inv = 1.f / l;
-      for (int c = 0; c < 256; c += 32) {
+    const long long urow = (((((long long)r * p.B + b) * p.Lq + i_q) * p.n_split + s_idx) * kHeads + h);
+    float* orow = p.dst_o + urow * kDv + 256 * cta + 128 * w;
+    const float l_tot = have ? sm.rsum[0][h] + sm.rsum[1][h] : 0.f;
+    if (have && l_tot > 0.f) {
+      const float inv = 1.f / l_tot;
+      for (int c = 0; c < 128; c += 32) {
         uint32_t v[32];
-        tmem_ld32(lane_addr + kColO + c, v);
+        tmem_ld32(lane_addr + kColO + 128 * w + c, v);
         tmem_wait_ld();
         float4* dst = reinterpret_cast<float4*>(orow + c);
 #pragma unroll
@@ -441,11 +462,11 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
           dst[k] = make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
                                __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
       }
-      if (cta == 0) p.dst_lse[urow] = (m_ref + log2f(l)) * 0.69314718055994531f;
+      if (cta == 0 && w == 0) p.dst_lse[urow] = (m_ref + log2f(l_tot)) * 0.69314718055994531f;
     } else {
       float4* dst = reinterpret_cast<float4*>(orow);
-      for (int k = 0; k < 64; ++k) dst[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (cta == 0) p.dst_lse[urow] = -INFINITY;
+      for (int k = 0; k < 32; ++k) dst[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (cta == 0 && w == 0) p.dst_lse[urow] = -INFINITY;
     }
   } else {
     // ---------------- score senders (warps 8..11), give registers up ----------------
@@ -456,7 +477,7 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
     const int lg = warp & 3;
     const int h = lg * 32 + lane;
     const uint32_t lane_addr = taddr(tmem, (uint32_t)(lg * 32), 0);
-    const uint32_t peer_x = mapa(smem_u32(xbuf + 4 * h), peer);   // chunk 0 of head h
+    const uint32_t peer_x = mapa(smem_u32(xbuf + 4 * h), peer);
     const uint32_t peer_recv_full = mapa(smem_u32(&sm.recv_full[0]), peer);
     bool ok = true;
     for (int t = 0; t < T; ++t) {
@@ -559,7 +580,7 @@ cudaError_t launch_attn_mla_tc(const AttnArgs& a, const SplitPlan& plan) {
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, mla_attn_kernel);
   if (e != cudaSuccess) return e;
-  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  if (fa.numRegs * (int)kThreads < kSplitRegs) return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(mla_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long long units = (long long)a.N * a.B * a.Lq * plan.n_split;
