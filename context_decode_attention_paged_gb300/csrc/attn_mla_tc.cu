@@ -15,16 +15,28 @@
 //   TMEM, streams the same dims of each 64-token KV tile (TMA, 128B/64B
 //   swizzle) and computes the partial score S_c = Q_c K_c^T (M=128 heads, N=64
 //   tokens, K=288; A from TMEM).  The two CTAs swap S_c through distributed
-//   shared memory, so both hold S = S_0 + S_1 (bit-identical: fp32 addition
-//   commutes) and run the same online softmax.  CTA c then accumulates output
-//   dims [256c, 256c+256) = O_c += P V_c (M=128, N=256, K=64; P from TMEM, V
-//   read MN-major from the latent part of its own KV tile).
+//   shared memory (16-byte st.async stores counted on the receiver's mbarrier,
+//   scores rounded to 24 bits), so both hold the same S = S_0 + S_1 and run the
+//   same online softmax.  CTA c then accumulates output dims [256c, 256c+256):
+//   O_c += P V_c (M=128, N=256, K=64; P from TMEM, V read MN-major from the
+//   latent part of its own KV tile).
 // Every KV byte is loaded once (each CTA loads its half of the dims) and no MMA
 // is repeated.  The softmax runs in the log2 domain with a lazily updated
-// reference max (rescale O only when the running max grows by more than 2^8).
+// reference max (O is rescaled only when the running max grows by > 2^8).
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
-// owner, warps 2..5 = softmax/epilogue, one query head (TMEM lane) per thread.
+// Warp roles (512 threads; setmaxnreg moves registers to the softmax warps):
+//   warp 0      TMA producer (4-stage ring of 36 KB tiles)
+//   warp 1      PV MMA issuer, TMEM owner
+//   warp 2      score (QK^T) MMA issuer - a separate thread, so the score tile of
+//               t+1 and its exchange never wait behind tile t's PV
+//   warp 3      idle
+//   warps 4-11  softmax / epilogue, two warpgroups: warpgroup w handles tokens
+//               [32w, +32) of every tile and output columns [128w, +128); they
+//               combine partial row maxima once per tile (bounded mbarrier);
+//               one-tile lookahead: tile t+1's scores leave TMEM before tile t's
+//               softmax, releasing S to the score MMA
+//   warps 12-15 score senders: read this CTA's partial scores out of TMEM and
+//               push them to the peer, so the softmax never stalls on the link
 // Every wait is bounded; on expiry the kernel records DCP_ERR_TIMEOUT, drains
 // its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
