@@ -16,6 +16,7 @@ the step's fraction of its HBM/tensor roofline and query-tokens/s alongside.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -67,6 +68,25 @@ def algorithmic(w: wl.Workload, seq_lens) -> dict:
             "merge_bytes": partials + out,
             "step_bytes": kv + q + 2 * partials + out,
             "flops": flops}
+
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one attention
+# launch, as a multiple of its algorithmic bytes, from the ncu captures
+# summarised in profiles/ (a smaller case of the same kernel; traffic scales
+# with the cache bytes processed).  Keyed by the kernel source the counters
+# were taken on: once the source changes, traffic is reported as null.
+NCU_TRAFFIC_RATIO = {
+    "mla": ("2d76a7d699e4db5f", 1.00893, "attn_mla_tc.cu"),   # mla_attn_kernel_mla32_full.md
+    "gqa": ("e1422c4cc8231f3a", 1.00410, "attn_gqa_tc.cu"),   # gqa_attn_kernel_qwen_full.md
+}
+
+
+def measured_traffic(kind: str, alg_bytes: int):
+    sha, ratio, fname = NCU_TRAFFIC_RATIO[kind]
+    path = os.path.join(ROOT, "context_decode_attention_paged_gb300", "csrc", fname)
+    with open(path, "rb") as f:
+        cur = hashlib.sha256(f.read()).hexdigest()[:16]
+    return int(round(ratio * alg_bytes)) if cur == sha else None
 
 
 def load_peaks():
@@ -364,7 +384,7 @@ def run_ours(args):
     else:
         roof = {"bound": "tensor", "achieved": round(attn_tfs, 1), "peak": tflops,
                 "unit": "TFLOP/s", "frac": round(attn_tfs / tflops, 4)}
-    roof.update({"traffic": None, "peak_source": f"{peak_src} (MEASURED_PEAKS.json)"
+    roof.update({"traffic": measured_traffic(w.kind, alg["attn_bytes"]), "peak_source": f"{peak_src} (MEASURED_PEAKS.json)"
                  if peak_src == "measured" else "fallback",
                  "kernel": "dcp_decode_attn", "attn_ms": round(attn_avg, 4),
                  "merge_ms": round(statistics.mean(merge_ms), 4),
