@@ -16,8 +16,8 @@
 //   swizzle) and computes the partial score S_c = Q_c K_c^T (M=128 heads, N=64
 //   tokens, K=288; A from TMEM).  The two CTAs swap S_c through distributed
 //   shared memory (16-byte st.async stores counted on the receiver's mbarrier,
-//   scores rounded to 24 bits), so both hold the same S = S_0 + S_1 and run the
-//   same online softmax.  CTA c then accumulates output dims [256c, 256c+256):
+//   16-bit block floating point), so both hold S = S_0 + S_1 (each with the
+//   peer's half quantised) and run the same online softmax.  CTA c then accumulates output dims [256c, 256c+256):
 //   O_c += P V_c (M=128, N=256, K=64; P from TMEM, V read MN-major from the
 //   latent part of its own KV tile).
 // Every KV byte is loaded once (each CTA loads its half of the dims) and no MMA
@@ -59,16 +59,19 @@ constexpr int kStages = 4;
 constexpr uint32_t kChunkBytes = kNt * 128;   // 64 tokens x 64 dims bf16, 128B rows
 constexpr uint32_t kRopeBytes = kNt * 64;     // 64 tokens x 32 dims bf16, 64B rows
 constexpr uint32_t kStageBytes = 4 * kChunkBytes + kRopeBytes;   // 36 KB
-// Exchange buffer: each head's 64 partial scores travel as 24-bit values (fp32
-// rounded to nearest on the low 8 mantissa bits, 4 values in 3 words), 192
-// bytes per head in 12 chunks of 16 bytes, chunk-major: chunk k of head h at
-// (k * 128 + h) * 16, so one warp's store (or load) of a chunk covers 512
-// contiguous bytes.  The DSMEM link moves ~15 B/clk per direction; 24-bit
-// scores cut the per-tile exchange from 32 KB to 24 KB.  Both CTAs round both
-// partials the same way before adding, so their softmax inputs stay
-// bit-identical; the score error is at most |s_partial| * 2^-17.
-constexpr int kXChunks = 12;
-constexpr uint32_t kXBytes = kHeads * kXChunks * 16;
+// Exchange buffer: each head's 64 partial scores travel as 16-bit integers
+// sharing one power-of-two scale per head and tile (block floating point):
+// 128 bytes per head in 8 chunks of 16 bytes, chunk-major (chunk k of head h
+// at (k * 128 + h) * 16, so one warp's store or load of a chunk covers 512
+// contiguous bytes), followed by the 128 per-head decode scales.  The DSMEM
+// link moves ~15 B/clk per direction, so the 16.5 KB exchange of a tile takes
+// ~1,100 cycles.  The scale maps the head's largest |partial| into [2^13, 2^14),
+// so each received partial is off by at most max|partial| * 2^-15; each CTA
+// adds its own partial unrounded (the two CTAs' softmax inputs differ in the
+// last bits; each CTA normalises its own half of the output with its own sums).
+constexpr int kXChunks = 8;
+constexpr uint32_t kXScoreBytes = kHeads * kXChunks * 16;   // 16 KB
+constexpr uint32_t kXBytes = kXScoreBytes + kHeads * 4;     // + one fp32 scale per head
 constexpr uint32_t kThreads = 512;             // 4 warpgroups
 // Register split (setmaxnreg) against the 384 x 168 registers of the launch:
 // control warpgroup and score senders give registers up, softmax takes them.
@@ -114,22 +117,28 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ uint32_t round24(float f) { return (__float_as_uint(f) + 0x80u) >> 8; }
-__device__ __forceinline__ float widen24(uint32_t b) { return __uint_as_float(b << 8); }
+// Block floating point for the score exchange.  Encoding adds 1.5 * 2^23 +
+// 2^15 to the scaled score: the fp32 sum holds round(score * enc) + 2^15 as an
+// integer in its low 16 bits.  Decoding places those bits under the exponent of
+// 2^23 and subtracts (2^23 + 2^15) * dec in one exact FMA.
+constexpr float kEncMagic = 12615680.0f;    // 1.5 * 2^23 + 2^15
+constexpr float kDecBias = 8421376.0f;      // 2^23 + 2^15
 
-// four scores -> three words (24 bits each)
-__device__ __forceinline__ void pack24(float a, float b, float c, float d, uint32_t& w0, uint32_t& w1, uint32_t& w2) {
-  const uint32_t b0 = round24(a), b1 = round24(b), b2 = round24(c), b3 = round24(d);
-  w0 = b0 | (b1 << 24);
-  w1 = (b1 >> 8) | (b2 << 16);
-  w2 = (b2 >> 16) | (b3 << 8);
+// enc = 2^(13 - e), dec = 2^(e - 13) for the exponent e of amax (clamped so both
+// stay normal), so |score| * enc < 2^14.
+__device__ __forceinline__ void bfp_scales(float amax, float& enc, float& dec) {
+  const int eb = min(max((int)(__float_as_uint(amax) >> 23), 30), 200);
+  enc = __uint_as_float((uint32_t)(267 - eb) << 23);
+  dec = __uint_as_float((uint32_t)(eb - 13) << 23);
 }
 
-__device__ __forceinline__ void unpack24(uint32_t w0, uint32_t w1, uint32_t w2, float* v) {
-  v[0] = widen24(w0 & 0xFFFFFFu);
-  v[1] = widen24((w0 >> 24) | ((w1 & 0xFFFFu) << 8));
-  v[2] = widen24((w1 >> 16) | ((w2 & 0xFFu) << 16));
-  v[3] = widen24(w2 >> 8);
+__device__ __forceinline__ uint32_t bfp_pack2(float a, float b, float enc) {
+  return __byte_perm(__float_as_uint(fmaf(a, enc, kEncMagic)), __float_as_uint(fmaf(b, enc, kEncMagic)), 0x5410);
+}
+
+// low (sel 0x7610) or high (sel 0x7632) 16-bit code of w, decoded
+__device__ __forceinline__ float bfp_unpack(uint32_t w, uint32_t sel, float dec, float bias) {
+  return fmaf(__uint_as_float(__byte_perm(w, 0x4B000000u, sel)), dec, bias);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -364,33 +373,35 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       if (mt == 0) mbar_arrive_expect_tx(smem_u32(&sm.recv_full[xb]), kXBytes);
       if (!wwait(smem_u32(&sm.recv_full[xb]), (uint32_t)(t >> 1) & 1u)) { ok = false; break; }
       {
-        const uint4* theirs = reinterpret_cast<const uint4*>(xbuf + xb * (kXBytes / 4)) + h;
-        uint32_t wd[24];
+        // peer's partial (tokens [32w, +32): chunks [4w, +4)) plus our own
+        const float* xrow = xbuf + xb * (kXBytes / 4);
+        const uint4* theirs = reinterpret_cast<const uint4*>(xrow) + h;
+        const float dec = xrow[kXScoreBytes / 4 + h];
+        const float bias = -kDecBias * dec;
 #pragma unroll
-        for (int k = 0; k < 6; ++k) {
-          const uint4 q4 = theirs[(6 * w + k) * kHeads];
-          wd[4 * k] = q4.x;
-          wd[4 * k + 1] = q4.y;
-          wd[4 * k + 2] = q4.z;
-          wd[4 * k + 3] = q4.w;
-        }
+        for (int k = 0; k < 4; ++k) {
+          const uint4 q4 = theirs[(4 * w + k) * kHeads];
+          const uint32_t wq[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          float o[4];
-          unpack24(wd[3 * g], wd[3 * g + 1], wd[3 * g + 2], o);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) x[4 * g + e] = widen24(round24(x[4 * g + e])) + o[e];
+          for (int j = 0; j < 4; ++j) {
+            x[8 * k + 2 * j] += bfp_unpack(wq[j], 0x7610u, dec, bias);
+            x[8 * k + 2 * j + 1] += bfp_unpack(wq[j], 0x7632u, dec, bias);
+          }
         }
       }
-      // online softmax, log2 domain; tree reductions keep dependency chains short
+      // online softmax in the log2 domain on raw scores (scale > 0 is folded
+      // into the exponent); tree reductions keep dependency chains short
       const int valid = min(kNt, ke - (kb + t * kNt)) - 32 * w;   // may be <= 0
+      const bool full = valid >= 32;
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (full) {
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        x[k] = (k < valid) ? x[k] * p.scale_log2 : -INFINITY;
-        m4[k & 3] = fmaxf(m4[k & 3], x[k]);
+        for (int k = 0; k < 32; ++k) m4[k & 3] = fmaxf(m4[k & 3], x[k]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) m4[k & 3] = fmaxf(m4[k & 3], (k < valid) ? x[k] : -INFINITY);
       }
-      const float pmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      const float pmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
       // post the partial max; the barrier also tells us both warpgroups have
       // read exchange buffer xb, so the peer may refill it
       sm.rmax[xb][w][h] = pmax;
@@ -405,14 +416,25 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
         alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - tmax);
         m_ref = tmax;
       }
+      const float sl2 = p.scale_log2, nm = -m_ref;
       uint32_t pk[16];
       float l4[4] = {0.f, 0.f, 0.f, 0.f};
+      if (full) {
 #pragma unroll
-      for (int k = 0; k < 32; k += 2) {
-        const float p0 = (k < valid) ? ex2(x[k] - m_ref) : 0.f;
-        const float p1 = (k + 1 < valid) ? ex2(x[k + 1] - m_ref) : 0.f;
-        l4[(k >> 1) & 3] += p0 + p1;
-        pk[k / 2] = pack_bf16x2(p0, p1);
+        for (int k = 0; k < 32; k += 2) {
+          const float p0 = ex2(fmaf(x[k], sl2, nm));
+          const float p1 = ex2(fmaf(x[k + 1], sl2, nm));
+          l4[(k >> 1) & 3] += p0 + p1;
+          pk[k / 2] = pack_bf16x2(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const float p0 = (k < valid) ? ex2(fmaf(x[k], sl2, nm)) : 0.f;
+          const float p1 = (k + 1 < valid) ? ex2(fmaf(x[k + 1], sl2, nm)) : 0.f;
+          l4[(k >> 1) & 3] += p0 + p1;
+          pk[k / 2] = pack_bf16x2(p0, p1);
+        }
       }
       l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
       // PV of the previous tile must be done before O is rescaled or P rewritten
@@ -481,7 +503,7 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       if (cta == 0 && w == 0) p.dst_lse[urow] = -INFINITY;
     }
   } else {
-    // ---------------- score senders (warps 8..11), give registers up ----------------
+    // ---------------- score senders (warps 12..15), give registers up ----------------
     // Each tile's partial scores go to the peer as 16-byte async stores that
     // count bytes on the peer's barrier; a dedicated warpgroup does it so the
     // softmax warps never stall on the DSMEM link.
@@ -489,7 +511,8 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
     const int lg = warp & 3;
     const int h = lg * 32 + lane;
     const uint32_t lane_addr = taddr(tmem, (uint32_t)(lg * 32), 0);
-    const uint32_t peer_x = mapa(smem_u32(xbuf + 4 * h), peer);
+    const uint32_t peer_x = mapa(smem_u32(xbuf + 4 * h), peer);                 // chunk 0 of head h
+    const uint32_t peer_xs = mapa(smem_u32(xbuf + kXScoreBytes / 4 + h), peer);  // scale of head h
     const uint32_t peer_recv_full = mapa(smem_u32(&sm.recv_full[0]), peer);
     bool ok = true;
     for (int t = 0; t < T; ++t) {
@@ -513,19 +536,44 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       }
       const uint32_t dst = peer_x + xb * kXBytes;
       const uint32_t bar = peer_recv_full + 8 * xb;
-      uint32_t wd[48];
+      // rows past the end of a ragged tile hold stale cache bytes: zero them so
+      // they cannot set the scale (the softmax masks them anyway)
+      const int tv = min(kNt, ke - (kb + t * kNt));
+      if (tv < kNt) {
 #pragma unroll
-      for (int g = 0; g < 8; ++g)
-        pack24(__uint_as_float(v0[4 * g]), __uint_as_float(v0[4 * g + 1]), __uint_as_float(v0[4 * g + 2]),
-               __uint_as_float(v0[4 * g + 3]), wd[3 * g], wd[3 * g + 1], wd[3 * g + 2]);
+        for (int k = 0; k < 32; ++k) {
+          if (k >= tv) v0[k] = 0u;
+          if (k + 32 >= tv) v1[k] = 0u;
+        }
+      }
+      float a8[8];
 #pragma unroll
-      for (int g = 0; g < 8; ++g)
-        pack24(__uint_as_float(v1[4 * g]), __uint_as_float(v1[4 * g + 1]), __uint_as_float(v1[4 * g + 2]),
-               __uint_as_float(v1[4 * g + 3]), wd[24 + 3 * g], wd[24 + 3 * g + 1], wd[24 + 3 * g + 2]);
+      for (int k = 0; k < 8; ++k) a8[k] = fmaxf(fabsf(__uint_as_float(v0[k])), fabsf(__uint_as_float(v1[k])));
 #pragma unroll
-      for (int k = 0; k < kXChunks; ++k)
-        st_async_v4(dst + k * (kHeads * 16), __uint_as_float(wd[4 * k]), __uint_as_float(wd[4 * k + 1]),
-                    __uint_as_float(wd[4 * k + 2]), __uint_as_float(wd[4 * k + 3]), bar);
+      for (int k = 8; k < 32; ++k)
+        a8[k & 7] = fmaxf(a8[k & 7], fmaxf(fabsf(__uint_as_float(v0[k])), fabsf(__uint_as_float(v1[k]))));
+      const float amax = fmaxf(fmaxf(fmaxf(a8[0], a8[1]), fmaxf(a8[2], a8[3])),
+                               fmaxf(fmaxf(a8[4], a8[5]), fmaxf(a8[6], a8[7])));
+      float enc, dec;
+      bfp_scales(amax, enc, dec);
+      // chunk k carries tokens [8k, 8k + 8): two per word
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        st_async_v4(dst + k * (kHeads * 16),
+                    __uint_as_float(bfp_pack2(__uint_as_float(v0[8 * k]), __uint_as_float(v0[8 * k + 1]), enc)),
+                    __uint_as_float(bfp_pack2(__uint_as_float(v0[8 * k + 2]), __uint_as_float(v0[8 * k + 3]), enc)),
+                    __uint_as_float(bfp_pack2(__uint_as_float(v0[8 * k + 4]), __uint_as_float(v0[8 * k + 5]), enc)),
+                    __uint_as_float(bfp_pack2(__uint_as_float(v0[8 * k + 6]), __uint_as_float(v0[8 * k + 7]), enc)),
+                    bar);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        st_async_v4(dst + (k + 4) * (kHeads * 16),
+                    __uint_as_float(bfp_pack2(__uint_as_float(v1[8 * k]), __uint_as_float(v1[8 * k + 1]), enc)),
+                    __uint_as_float(bfp_pack2(__uint_as_float(v1[8 * k + 2]), __uint_as_float(v1[8 * k + 3]), enc)),
+                    __uint_as_float(bfp_pack2(__uint_as_float(v1[8 * k + 4]), __uint_as_float(v1[8 * k + 5]), enc)),
+                    __uint_as_float(bfp_pack2(__uint_as_float(v1[8 * k + 6]), __uint_as_float(v1[8 * k + 7]), enc)),
+                    bar);
+      st_async_b32(peer_xs + xb * kXBytes, __float_as_uint(dec), bar);
     }
     if (!ok) fail();
   }

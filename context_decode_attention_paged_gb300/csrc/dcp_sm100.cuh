@@ -57,6 +57,12 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
                :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar) : "memory");
 }
 
+// 4-byte variant of st_async_v4.
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+               :: "r"(addr), "r"(v), "r"(cluster_bar) : "memory");
+}
+
 // Named barrier over `count` threads (multiple of 32); id 0 is __syncthreads.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
