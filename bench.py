@@ -76,7 +76,7 @@ def algorithmic(w: wl.Workload, seq_lens) -> dict:
 # with the cache bytes processed).  Keyed by the kernel source the counters
 # were taken on: once the source changes, traffic is reported as null.
 NCU_TRAFFIC_RATIO = {
-    "mla": ("2d76a7d699e4db5f", 1.00893, "attn_mla_tc.cu"),   # mla_attn_kernel_mla32_full.md
+    "mla": ("7033720de13ca2df", 1.00889, "attn_mla_tc.cu"),   # mla_attn_kernel_mla32_full.md
     "gqa": ("e1422c4cc8231f3a", 1.00410, "attn_gqa_tc.cu"),   # gqa_attn_kernel_qwen_full.md
 }
 
