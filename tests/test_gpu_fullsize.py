@@ -1,0 +1,77 @@
+"""GPU parity at the full sizes of the workload configurations, in the launch
+configuration bench.py times.
+
+The whole decode step (all shards, one attention launch, one merge launch) runs
+on the device over the full synthetic workload, generated exactly as the
+benchmark generates it.  A few requests are then checked element by element
+against the oracle, which is run for those requests alone on a compact host
+copy of their cache blocks; properties that hold at any size are checked on
+every output: everything finite, every partial LSE finite (every shard of these
+workloads has keys), and every output bounded by the largest |entry| of the
+value cache (the output is a convex combination of value rows).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import bench
+from context_decode_attention_paged_gb300 import workloads as wl
+from gpu_common import assert_close, assert_lse_close
+from oracle import dcp_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+FULL = ["qwen_gqa", "mla_32", "mla_mtp", "mla_512"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from context_decode_attention_paged_gb300 import build
+    build.build()
+
+
+def _sampled_requests(w: wl.Workload):
+    if w.batch == 1:
+        return [0]
+    rng = np.random.default_rng(20260 + w.batch)
+    extra = rng.choice(np.arange(1, w.batch - 1), size=1, replace=False).tolist()
+    return sorted({0, w.batch - 1, *extra})
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_against_oracle(name):
+    from context_decode_attention_paged_gb300 import binding as dcp
+    w = wl.WORKLOADS[name]
+    inst = bench.setup_gpu(w, 0)
+    try:
+        po, lse = dcp.dcp_decode_attn(w.kind, inst.q, inst.kv_cache, inst.block_tables, inst.seq_lens,
+                                      w.dcp_size, w.interleave, w.scale, w.q_len, w.head_dim_v)
+        out, out_lse = dcp.dcp_merge(po, lse, w.dcp_size)
+        torch.cuda.synchronize()
+        assert dcp.dcp_get_last_device_status() == dcp.DCP_OK
+
+        # properties over every output
+        assert torch.isfinite(po).all() and torch.isfinite(lse).all()
+        assert torch.isfinite(out.float()).all() and torch.isfinite(out_lse).all()
+        vals = inst.kv_cache[1] if w.kind == "gqa" else inst.kv_cache     # (MLA: latent and rope)
+        vmax = torch.maximum(vals.amax().float().abs(), vals.amin().float().abs())
+        assert out.float().abs().max() <= vmax * (1 + 1e-2)
+
+        # sampled requests, element by element
+        idx = _sampled_requests(w)
+        q, kv, bt, sl = bench.host_sample(inst, idx)
+        ref = orc.ref_dcp_decode(w.kind, orc.to_f64(q), orc.to_f64(kv), bt, sl, w.dcp_size, w.interleave,
+                                 w.block_size, w.scale, w.q_len, w.head_dim_v)
+        sel = torch.as_tensor(idx, device=po.device)
+        assert_close(out.index_select(1, sel).float().cpu().numpy(), ref["out"], f"{name} out")
+        assert_lse_close(out_lse.index_select(1, sel).cpu().numpy(), ref["out_lse"], f"{name} out_lse")
+        assert_close(po.index_select(1, sel).cpu().numpy(), ref["partial_out"], f"{name} partial_out")
+        assert_lse_close(lse.index_select(1, sel).cpu().numpy(), ref["lse"], f"{name} lse")
+    finally:
+        del inst
+        torch.cuda.empty_cache()
