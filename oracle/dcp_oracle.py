@@ -153,6 +153,47 @@ def ref_attn_unsharded(q, keys, values, seq_lens, scale: float, q_len: int):
 
 
 # ---------------------------------------------------------------------------
+# Storing new tokens into the sharded cache (the step before the Compute step)
+# ---------------------------------------------------------------------------
+
+def ref_kv_cache_write(kind: str, kv_cache, new_k, new_v, block_tables, seq_lens,
+                       dcp_size: int, interleave: int, block_size: int, n_new: int):
+    """The cache after storing the newest n_new tokens of every request.
+
+    "Context Parallel Guide", section "Overview": DCP shards the KV cache
+    storage among the ranks of the DCP group, so each new token's KV row is
+    stored once, in the shard that owns its position (section "Decode Context
+    Parallel": the interleave flag; blog, section "解碼上下文並行 (DCP) 原理解析":
+    each rank holds a range of token positions).  Token i of request b sits at
+    global position t = seq_lens[b] - n_new + i (seq_lens count the new
+    tokens); its shard r and local index j come from enumerating the shard's
+    positions (shard_token_lists); its slot is block_tables[r][b][j // bs],
+    row j % bs.
+
+    kind 'gqa': kv_cache [2][nb][bs][Hkv][D], new_k/new_v [B][n_new][Hkv][D]
+    kind 'mla': kv_cache [nb][bs][Dqk],      new_k [B][n_new][Dqk], new_v None
+    Returns a new array; the input cache is not modified.
+    """
+    out = np.array(kv_cache, copy=True)
+    bt = np.asarray(block_tables)
+    for b, S in enumerate(int(x) for x in seq_lens):
+        lists = shard_token_lists(S, interleave, dcp_size)
+        where = {}
+        for r, toks in enumerate(lists):
+            for j, t in enumerate(toks[max(0, len(toks) - n_new):].tolist(), start=max(0, len(toks) - n_new)):
+                where[t] = (r, j)
+        for i in range(n_new):
+            r, j = where[S - n_new + i]
+            blk, row = int(bt[r, b, j // block_size]), j % block_size
+            if kind == "gqa":
+                out[0, blk, row] = new_k[b, i]
+                out[1, blk, row] = new_v[b, i]
+            else:
+                out[blk, row] = new_k[b, i]
+    return out
+
+
+# ---------------------------------------------------------------------------
 # Per-shard partial attention read through the paged pool (Compute step)
 # ---------------------------------------------------------------------------
 
