@@ -187,6 +187,48 @@ def step_fn(inst, po, lse, out, out_lse, ws):
     return attn, merge
 
 
+def kv_write_timing(inst, reps: int):
+    """dcp_kv_cache_write of one decode step's new tokens (B x Lq rows), timed on
+    its own with CUDA events (the step before attention; not part of `value`)."""
+    from context_decode_attention_paged_gb300 import binding as dcp
+    w = inst.w
+    dev = inst.kv_cache.device
+    g = torch.Generator(device=dev).manual_seed(w.seed + 7)
+    if w.kind == "gqa":
+        shape = (w.batch, w.q_len, w.num_kv_heads, w.head_dim_qk)
+        new_k = torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
+        new_v = torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
+        row_bytes = 2 * w.num_kv_heads * w.head_dim_qk * 2          # K and V rows of a token
+    else:
+        new_k = torch.randn((w.batch, w.q_len, w.head_dim_qk), generator=g, device=dev).to(torch.bfloat16)
+        new_v = None
+        row_bytes = w.head_dim_qk * 2
+
+    def call():
+        dcp.dcp_kv_cache_write(w.kind, new_k, new_v, inst.kv_cache, inst.block_tables, inst.seq_lens,
+                               w.dcp_size, w.interleave)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    st = dcp.dcp_get_last_device_status()
+    if st != dcp.DCP_OK:
+        raise RuntimeError(f"device status after the cache write: {dcp.status_string(st)}")
+    ms = e0.elapsed_time(e1) / reps
+    rows = w.batch * w.q_len
+    alg = 2 * rows * row_bytes                                          # rows read + cells written
+    return {"kernel": "dcp_kv_cache_write", "ms_per_call": round(ms, 5), "tokens": rows,
+            "alg_bytes": alg, "achieved_gbs": round(alg / (ms * 1e-3) / 1e9, 2),
+            "reps": reps, "bound": "launch latency (a step writes a few hundred KB)"}
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -365,6 +407,8 @@ def run_ours(args):
     h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
 
+    kv_write = kv_write_timing(inst, reps=max(args.steps, 20))
+
     ms_per_step = max_over_ranks(total_ms / args.steps, world)
     e2e_ms = max_over_ranks(e2e_ms, world)
     kv_all = sum_over_ranks(float(alg["kv_bytes"]), world)
@@ -411,6 +455,7 @@ def run_ours(args):
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
+        "kv_write": kv_write,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         secs, kvb, nseq, qtok = oracle_time(inst, args.cpu_budget, args.cpu_max_seqs)

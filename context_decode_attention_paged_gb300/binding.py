@@ -47,6 +47,9 @@ _lib.dcp_decode_attn.argtypes = [ctypes.POINTER(DcpAttnDesc), _vp, _vp, _vp, _vp
 _lib.dcp_decode_attn_noalloc.restype = _i32
 _lib.dcp_decode_attn_noalloc.argtypes = [ctypes.POINTER(DcpAttnDesc), _vp, _vp, _vp, _vp, _i32,
                                          _i32, _f32, _i32, _vp, _vp, _vp]
+_lib.dcp_kv_cache_write.restype = _i32
+_lib.dcp_kv_cache_write.argtypes = [ctypes.POINTER(DcpAttnDesc), _vp, _vp, _vp, _vp, _vp, _i32, _i32,
+                                    _i32, _vp]
 _lib.dcp_merge.restype = _i32
 _lib.dcp_merge.argtypes = [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]
 _lib.dcp_get_last_device_status.restype = _i32
@@ -149,6 +152,24 @@ def dcp_decode_attn_noalloc(kind, q, kv_cache, block_tables, seq_lens, dcp_size,
                                         float(scale), causal_q_len, _ptr(partial_out), _ptr(lse),
                                         _stream(stream)), "dcp_decode_attn_noalloc")
     return partial_out, lse
+
+
+def dcp_kv_cache_write(kind, new_k, new_v, kv_cache, block_tables, seq_lens, dcp_size, interleave,
+                       stream=None):
+    """Store the newest n_new tokens of every request in their shards' cache cells
+    (kv_cache is written in place).  new_k/new_v: GQA [B][n_new][Hkv][D];
+    MLA new_k [B][n_new][Dqk] and new_v None."""
+    B, n_new = new_k.shape[0], new_k.shape[1]
+    if KINDS.get(kind, kind) == DCP_ATTN_GQA:
+        _, nb, bs, Hkv, D = kv_cache.shape
+    else:
+        nb, bs, D = kv_cache.shape
+        Hkv = 1
+    desc = make_desc(kind, B, n_new, Hkv, Hkv, D, D, bs, nb, block_tables.shape[2])
+    _check(_lib.dcp_kv_cache_write(ctypes.byref(desc), _ptr(new_k), _ptr(new_v), _ptr(kv_cache),
+                                   _ptr(block_tables), _ptr(seq_lens), dcp_size, interleave, n_new,
+                                   _stream(stream)), "dcp_kv_cache_write")
+    return kv_cache
 
 
 def dcp_merge(partial_out, lse, dcp_size, out=None, out_lse=None, want_lse=True, stream=None):

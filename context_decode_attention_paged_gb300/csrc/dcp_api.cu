@@ -205,6 +205,31 @@ dcp_status_t dcp_decode_attn(const dcp_attn_desc_t* d, const void* q, const void
   }
 }
 
+dcp_status_t dcp_kv_cache_write(const dcp_attn_desc_t* d, const void* new_k, const void* new_v,
+                                void* kv_cache, const int32_t* block_tables, const int32_t* seq_lens,
+                                int32_t dcp_size, int32_t interleave, int32_t n_new, void* stream) {
+  if (!d || !new_k || !kv_cache || !block_tables || !seq_lens) return DCP_ERR_INVALID_ARG;
+  if (d->kind != DCP_ATTN_GQA && d->kind != DCP_ATTN_MLA) return DCP_ERR_INVALID_ARG;
+  const bool gqa = d->kind == DCP_ATTN_GQA;
+  if (gqa != (new_v != nullptr)) return DCP_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->num_kv_heads < 1 || d->head_dim_qk < 1 || d->block_size < 1 || d->num_blocks < 1 ||
+      d->max_local_blocks < 1 || dcp_size < 1 || interleave < 1 || n_new < 1)
+    return DCP_ERR_INVALID_ARG;
+  if (!gqa && d->num_kv_heads != 1) return DCP_ERR_INVALID_ARG;
+  const long long row_bytes = 2LL * d->head_dim_qk * (gqa ? d->num_kv_heads : 1);
+  if (row_bytes % 16 || row_bytes > (1LL << 20)) return DCP_ERR_INVALID_ARG;
+  if ((long long)d->batch * dcp_size * d->max_local_blocks > (1LL << 31) ||
+      (long long)d->num_blocks * d->block_size > (1LL << 31))
+    return DCP_ERR_INVALID_ARG;
+  if (!aligned(new_k, 16) || !aligned(kv_cache, 16) || (new_v && !aligned(new_v, 16)))
+    return DCP_ERR_INVALID_ARG;
+  int* st = status_ptr();
+  if (!st) return DCP_ERR_CUDA;
+  return from_cuda(launch_kv_write(new_k, new_v, kv_cache, block_tables, seq_lens, d->batch, n_new, dcp_size,
+                                   interleave, d->block_size, d->max_local_blocks, d->num_blocks,
+                                   (int)row_bytes, st, static_cast<cudaStream_t>(stream)));
+}
+
 dcp_status_t dcp_merge(const float* partial_out, const float* lse, int32_t dcp_size,
                        int32_t batch, int32_t q_len, int32_t num_q_heads, int32_t head_dim_v,
                        void* out, float* out_lse, void* stream) {

@@ -50,6 +50,11 @@ cudaError_t launch_slot_map(const int32_t* seq_lens, int B, int bs, int I, int N
 cudaError_t launch_merge(const float* partial_out, const float* lse, int N, int B, int Lq,
                          int Hq, int Dv, void* out, float* out_lse, cudaStream_t stream);
 
+// Store the newest n_new tokens of every request in their shards' cache cells.
+cudaError_t launch_kv_write(const void* new_k, const void* new_v, void* kv_cache, const int32_t* block_tables,
+                            const int32_t* seq_lens, int B, int n_new, int N, int I, int bs, int max_lb,
+                            int num_blocks, int row_bytes, int* status, cudaStream_t stream);
+
 // Combine n_split workspace partials into partial_out / lse (row a5).
 cudaError_t launch_split_combine(const AttnArgs& a, const SplitPlan& p);
 

@@ -185,6 +185,36 @@ DCP_API dcp_status_t dcp_decode_attn_noalloc(const dcp_attn_desc_t* d, const voi
                                              int32_t causal_q_len, float* partial_out, float* lse,
                                              void* stream);
 
+/* Storing the newest tokens of every request in the sharded cache (the step
+ * before a2-a5 of a decode step).
+ * Source: "Context Parallel Guide", section "Overview" (DCP shards the KV cache
+ * storage among the ranks of the DCP group, so a token's KV is stored once, by
+ * the rank owning its position) and section "Decode Context Parallel" (the
+ * interleave flag); vLLM DCP blog, "解碼上下文並行 (DCP) 原理解析" (each rank
+ * holds a range of token positions).
+ * Token i of request b (0 <= i < n_new) has position t = seq_lens[b] - n_new + i
+ * (seq_lens already count the new tokens); its row goes to shard r = shard(t),
+ * local index j = local(t), i.e. block block_tables[r][b][j / block_size],
+ * slot j % block_size - the cells dcp_decode_attn reads it from.
+ *  d             shape: kind, batch, num_kv_heads, head_dim_qk, block_size,
+ *                num_blocks, max_local_blocks are used
+ *  new_k         bf16, GQA [B][n_new][Hkv][Dqk]; MLA [B][n_new][Dqk] (the row)
+ *  new_v         bf16, GQA [B][n_new][Hkv][Dqk]; MLA must be NULL
+ *  kv_cache      bf16, as in dcp_decode_attn; written in place (only the
+ *                B * n_new target rows of each pool)
+ *  block_tables  [dcp][B][max_local_blocks];  seq_lens [B]
+ * Alignment: new_k, new_v, kv_cache 16 bytes; a token row (Hkv * Dqk bf16,
+ * MLA Dqk) must be a multiple of 16 bytes.
+ * Errors: INVALID_ARG (NULL pointers, sizes < 1, new_v NULL for GQA or set for
+ * MLA, row size or alignment); on the device, a seq_len < n_new, a local index
+ * past the block table or a block id >= num_blocks sets DCP_ERR_BOUNDS and
+ * that token is skipped.                                                      */
+DCP_API dcp_status_t dcp_kv_cache_write(const dcp_attn_desc_t* d, const void* new_k,
+                                        const void* new_v, void* kv_cache,
+                                        const int32_t* block_tables, const int32_t* seq_lens,
+                                        int32_t dcp_size, int32_t interleave, int32_t n_new,
+                                        void* stream);
+
 /* Synchronises `stream`, returns the device status word set by earlier kernels
  * (DCP_OK if none) and clears it. */
 DCP_API dcp_status_t dcp_get_last_device_status(void* stream);

@@ -30,7 +30,7 @@ def test_header_declares_the_calls():
     syms = declared_symbols()
     for s in ("dcp_build_slot_map", "dcp_decode_attn", "dcp_merge",
               "dcp_decode_attn_workspace_size", "dcp_get_last_device_status",
-              "dcp_status_string"):
+              "dcp_status_string", "dcp_kv_cache_write"):
         assert s in syms
 
 
@@ -122,3 +122,28 @@ def test_slot_map_rejects_bad_arguments(lib):
 
 def test_workspace_size_of_invalid_desc_is_zero(lib):
     assert lib.dcp_decode_attn_workspace_size(_desc(lib, num_q_heads=7), 2) == 0
+
+
+def _kvw(lib, desc, new_k=FAKE, new_v=FAKE, cache=FAKE, dcp_size=2, interleave=16, n_new=1):
+    raw = lib.raw_lib()
+    return raw.dcp_kv_cache_write(ctypes.byref(desc), new_k, new_v, cache, FAKE, FAKE, dcp_size,
+                                  interleave, n_new, None)
+
+
+@pytest.mark.parametrize("kw,extra", [
+    ({}, dict(new_v=None)),                                        # GQA needs the V rows
+    (dict(kind="mla", num_kv_heads=1, head_dim_qk=576, head_dim_v=512), {}),   # MLA takes no V
+    (dict(kind="mla", num_kv_heads=2, head_dim_qk=576, head_dim_v=512), dict(new_v=None)),
+    ({}, dict(n_new=0)),
+    ({}, dict(dcp_size=0)),
+    ({}, dict(interleave=0)),
+    (dict(batch=0), {}),
+    (dict(block_size=0), {}),
+    (dict(num_blocks=0), {}),
+    (dict(num_kv_heads=1, head_dim_qk=4, head_dim_v=4), {}),       # 8-byte rows
+    ({}, dict(new_k=ctypes.c_void_p(0x10008))),                    # misaligned
+    ({}, dict(cache=None)),
+    (dict(kind=7), {}),
+])
+def test_kv_cache_write_rejects_bad_arguments(lib, kw, extra):
+    assert _kvw(lib, _desc(lib, **kw), **extra) == lib.DCP_ERR_INVALID_ARG
