@@ -5,11 +5,13 @@
 // section "Grouped-Query Attention (GQA) 後端" (query heads grouped over a few
 // KV heads; query head h reads KV head h / (Hq / Hkv)).
 //
-// Work unit = (shard r, request b, KV head g, KV split s), one CTA.  The query
-// rows of KV head g - (query i, head of the group), R = Lq * Hq / Hkv of them -
-// are the M dimension of the MMAs, padded to 128: the path moves 16 flop per
-// cache byte, far below the tensor pipe's ridge, so the padding costs tensor
-// time that is idle anyway and keeps one row per TMEM lane.
+// Work unit = (shard r, request b, KV head g, row tile m, KV split s), one CTA.
+// The query rows of KV head g - (query i, head of the group), Lq * Hq / Hkv of
+// them - are the M dimension of the MMAs, 128 per row tile (padded): the path
+// moves 16 flop per cache byte, far below the tensor pipe's ridge, so the
+// padding costs tensor time that is idle anyway and keeps one row per TMEM
+// lane.  Long causal queries (chunked prefill) take several row tiles, each
+// streaming the shard's keys.
 //   S = Q K^T   (M=128, N=64 tokens, K=D; Q from TMEM, K tile K-major, 128B swizzle)
 //   O += P V    (M=128, N=D, K=64; P from TMEM, V tile read MN-major)
 // K and V tiles of 64 tokens stream through a TMA ring; a 3-D tensor map over
@@ -52,6 +54,7 @@ struct GqaParams {
   float* dst_lse;
   int* status;
   int B, Lq, Hq, Hkv, N, I, max_lb, bs, num_blocks, n_split, split_tokens;
+  int m_tiles;         // row tiles of 128 query rows per KV head
   int D;               // head dim (64 or 128)
   int stages;
   float scale_log2;
@@ -84,21 +87,26 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long unit = blockIdx.x;
   const int s_idx = (int)(unit % p.n_split);
-  const int g = (int)((unit / p.n_split) % p.Hkv);
-  const int b = (int)((unit / ((long long)p.n_split * p.Hkv)) % p.B);
-  const int r = (int)(unit / ((long long)p.n_split * p.Hkv * p.B));
+  const int mt = (int)((unit / p.n_split) % p.m_tiles);
+  const long long gu = unit / ((long long)p.n_split * p.m_tiles);
+  const int g = (int)(gu % p.Hkv);
+  const int b = (int)((gu / p.Hkv) % p.B);
+  const int r = (int)(gu / ((long long)p.Hkv * p.B));
   const int gsize = p.Hq / p.Hkv;
-  const int R = p.Lq * gsize;                             // real query rows (<= 128)
+  const int row0 = 128 * mt;                              // first query row of this tile
+  const int R = min(128, p.Lq * gsize - row0);            // real query rows of this tile
   const int n_act = (R + 31) / 32;                        // softmax warps holding real rows
 
-  // key range (the last query sees the most keys; earlier queries mask)
+  // key range: the tile's last query sees the most keys; earlier queries mask
   const int S = p.seq_lens[b];
   const bool bad_len = S < p.Lq;
   int L = bad_len ? 0 : local_len(S, r, p.I, p.N);
   const bool short_table = (long long)L > (long long)p.max_lb * p.bs;
   if (short_table) L = p.max_lb * p.bs;
-  const int kb = min(L, s_idx * p.split_tokens);
-  const int ke = min(L, kb + p.split_tokens);
+  const int i_last = (row0 + R - 1) / gsize;
+  const int vis = bad_len ? 0 : min(L, local_count_upto((long long)S - p.Lq + i_last, r, p.I, p.N));
+  const int kb = min(vis, s_idx * p.split_tokens);
+  const int ke = min(vis, kb + p.split_tokens);
   const int T = (ke - kb + kNt - 1) / kNt;
   if (tid == 0 && (bad_len || short_table)) set_status(p.status, DCP_ERR_BOUNDS);
 
@@ -127,7 +135,7 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const bool real = row < R && !bad_len;
     const uint4* qrow = nullptr;
     if (real) {
-      const int i = row / gsize, head = g * gsize + row % gsize;
+      const int i = (row0 + row) / gsize, head = g * gsize + (row0 + row) % gsize;
       qrow = reinterpret_cast<const uint4*>(p.q + (((long long)b * p.Lq + i) * p.Hq + head) * p.D);
     }
     for (int c = 0; c < p.D / 32; ++c) {                  // 16 columns = 32 dims per store
@@ -241,8 +249,8 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const int lg = warp & 3;
     const int row = lg * 32 + lane;
     const bool real = row < R;
-    const int i_q = real ? row / gsize : 0;
-    const int head = g * gsize + (real ? row % gsize : 0);
+    const int i_q = real ? (row0 + row) / gsize : 0;
+    const int head = g * gsize + (real ? (row0 + row) % gsize : 0);
     const uint32_t lane_addr = taddr(tmem, (uint32_t)(lg * 32), 0);
     // causal limit of this row's query: a prefix of the shard-local keys
     const int lim = real ? min(ke, local_count_upto((long long)S - p.Lq + i_q, r, p.I, p.N)) : kb;
@@ -371,14 +379,16 @@ size_t gqa_smem_bytes(int D, int stages) {
 
 bool gqa_tc_supported(const AttnArgs& a) {
   if (a.kind != DCP_ATTN_GQA || (a.Dqk != 64 && a.Dqk != 128) || a.Dv != a.Dqk) return false;
-  if ((long long)a.Lq * (a.Hq / a.Hkv) > 128) return false;
+  if ((long long)a.Lq * (a.Hq / a.Hkv) > (1LL << 20)) return false;
   if (a.bs % 8) return false;
   if (a.bs >= kNt ? (a.bs % kNt) : (kNt % a.bs)) return false;
   return (long long)a.num_blocks * a.bs < (1LL << 31);
 }
 
+static int gqa_m_tiles(const AttnArgs& a) { return (int)(((long long)a.Lq * (a.Hq / a.Hkv) + 127) / 128); }
+
 SplitPlan plan_attn_gqa_tc(const AttnArgs& a, int sm_count) {
-  return plan_splits(a, sm_count, kNt, a.Hkv);
+  return plan_splits(a, sm_count, kNt, a.Hkv * gqa_m_tiles(a));
 }
 
 cudaError_t launch_attn_gqa_tc(const AttnArgs& a, const SplitPlan& plan) {
@@ -408,6 +418,7 @@ cudaError_t launch_attn_gqa_tc(const AttnArgs& a, const SplitPlan& plan) {
   p.num_blocks = a.num_blocks;
   p.n_split = plan.n_split;
   p.split_tokens = plan.split_tokens;
+  p.m_tiles = gqa_m_tiles(a);
   p.D = a.Dqk;
   p.stages = kMaxStages;
   p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -423,7 +434,7 @@ cudaError_t launch_attn_gqa_tc(const AttnArgs& a, const SplitPlan& plan) {
   const size_t smem = gqa_smem_bytes(p.D, p.stages);
   cudaError_t e = cudaFuncSetAttribute(gqa_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const long long units = (long long)a.N * a.B * a.Hkv * plan.n_split;
+  const long long units = (long long)a.N * a.B * a.Hkv * p.m_tiles * plan.n_split;
   if (units == 0) return cudaSuccess;
   gqa_attn_kernel<<<(unsigned)units, kThreads, smem, a.stream>>>(tm_k, tm_v, p);
   e = cudaGetLastError();
