@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # ---------------------------------------------------------------------------
-# roofline arithmetic (per unit of work)
+# roofline arithmetic (per unit of work: cache bytes per token, fixed bytes per launch)
 # ---------------------------------------------------------------------------
 
 def kv_bytes_per_token(w: wl.Workload) -> int:

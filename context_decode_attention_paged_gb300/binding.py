@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_PKG, "libdcp.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libdcp.so is not built ({LIB_PATH}); run "
-                      "`python -c 'import __graft_entry__ as g; g.build()'`")
+                      "`python -m context_decode_attention_paged_gb300.build`")
 
 _lib = ctypes.CDLL(LIB_PATH)
 

@@ -50,7 +50,7 @@ extern "C" {
 typedef enum {
   DCP_OK = 0,
   DCP_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or shape          */
-  DCP_ERR_UNSUPPORTED = 2,  /* valid request this build has no kernel for     */
+  DCP_ERR_UNSUPPORTED = 2,  /* valid request the library has no kernel for   */
   DCP_ERR_CUDA = 3,         /* a CUDA runtime call failed                      */
   DCP_ERR_TIMEOUT = 4,      /* a device-side bounded wait expired              */
   DCP_ERR_BOUNDS = 5        /* device-side range check failed (see above)     */

@@ -27,7 +27,7 @@ What the method computes, and where the pages say so
   rule used here is shard(t) = (t // interleave) % dcp_size, which the worked
   example above is the interleave = 50K, dcp_size = 4 case of.
 
-Readings where the pages are silent (each is repeated in the design doc):
+Readings where the pages are silent:
 * tokens of one shard are stored densely in increasing global order;
 * seq_len counts the query tokens (their KV is already cached); query i of a
   request of length S sits at position S - Lq + i and sees keys at positions
