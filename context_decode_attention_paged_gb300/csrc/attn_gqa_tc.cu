@@ -7,21 +7,30 @@
 //
 // Work unit = (shard r, request b, KV head g, row tile m, KV split s), one CTA.
 // The query rows of KV head g - (query i, head of the group), Lq * Hq / Hkv of
-// them - are the M dimension of the MMAs, 128 per row tile (padded): the path
-// moves 16 flop per cache byte, far below the tensor pipe's ridge, so the
-// padding costs tensor time that is idle anyway and keeps one row per TMEM
-// lane.  Long causal queries (chunked prefill) take several row tiles, each
-// streaming the shard's keys.
-//   S = Q K^T   (M=128, N=64 tokens, K=D; Q from TMEM, K tile K-major, 128B swizzle)
-//   O += P V    (M=128, N=D, K=64; P from TMEM, V tile read MN-major)
-// K and V tiles of 64 tokens stream through a TMA ring; a 3-D tensor map over
-// the pool [block*block_size][Hkv][D] selects KV head g, so any block size
-// that is a multiple of 8 works (small blocks take several boxes per tile).
-// Softmax: one thread per query row, log2 domain, lazily rescaled reference
-// max; the causal limit of query i is a prefix of the shard-local keys.
+// them - are few (16 for one decode token of a 16-head group), so the kernel
+// computes the transposed products and puts the KEYS on the 128 rows of the
+// MMA, one key per TMEM lane and per softmax thread:
+//   S^T = K Q^T    (M = 128 keys, N = NCOL query rows, K = D;
+//                   K tile K-major and Q^T K-major, both 128B-swizzled smem)
+//   O^T += V^T P^T (M = 128 value dims, N = NCOL, K = 128 keys;
+//                   V tile read MN-major from the same stage, P^T MN-major smem)
+// NCOL is 16, 32 or 64 (the tile's query rows, padded); longer causal queries
+// (chunked prefill) take several row tiles, each streaming the shard's keys.
+// K and V tiles of 128 tokens stream through a TMA ring; a 3-D tensor map over
+// the pool [block*block_size][Hkv][D] selects KV head g, so any block size that
+// is a multiple of 8 and divides (or is a multiple of) 128 works.
+//
+// Softmax: thread k of the four softmax warps owns key k of the tile and the
+// scores of that key for every query row.  The reference max of each row is
+// shared by all threads and moves lazily: one barrier per tile ORs "some score
+// exceeds its row's reference by more than 2^8"; only then do the warps reduce
+// the tile's row maxima, rescale O^T (after the previous PV has landed) and
+// their per-thread row sums.  Row sums are reduced across the 128 key threads
+// once, at the end.  Logs are base 2 with the scale folded into the exponent.
 // Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner, warps 2..5 softmax/epilogue (those holding real rows).  Every wait is
-// bounded; on expiry the kernel records DCP_ERR_TIMEOUT and unwinds.
+// owner, warps 2..5 softmax/epilogue.  Every wait is bounded; on expiry the
+// kernel records DCP_ERR_TIMEOUT and unwinds, the softmax warps deciding
+// together (barrier-reduced predicates) so that none is left at a barrier.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -35,16 +44,15 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kNt = 64;                        // tokens per tile
+constexpr int kNt = 128;                       // keys per tile (MMA M of S^T)
 constexpr int kMaxStages = 6;
-constexpr uint32_t kChunkBytes = kNt * 128;    // 64 tokens x 64 dims bf16
+constexpr uint32_t kChunkBytes = kNt * 128;    // 128 keys x 64 dims bf16
 constexpr uint32_t kThreads = 192;
 constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr uint32_t kColQ = 0;                  // D/2 columns (bf16 pairs)
-constexpr uint32_t kColP = 64;                 // 32 columns
-constexpr uint32_t kColS = 128;                // 64 columns fp32
-constexpr uint32_t kColO = 256;                // D columns fp32
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kMaxCols = 64;                   // query rows per row tile
+constexpr size_t kSmemLimit = 232448;          // dynamic shared memory per CTA
+constexpr uint32_t kBarSoftmax = 1;            // named barrier of the softmax warps
 
 struct GqaParams {
   const __nv_bfloat16* q;
@@ -54,7 +62,7 @@ struct GqaParams {
   float* dst_lse;
   int* status;
   int B, Lq, Hq, Hkv, N, I, max_lb, bs, num_blocks, n_split, split_tokens;
-  int m_tiles;         // row tiles of 128 query rows per KV head
+  int m_tiles;         // row tiles of NCOL query rows per KV head
   int D;               // head dim (64 or 128)
   int stages;
   float scale_log2;
@@ -63,9 +71,11 @@ struct GqaParams {
 struct Smem {
   uint64_t kv_full[kMaxStages];
   uint64_t kv_empty[kMaxStages];
-  uint64_t s_full, s_free, p_full, pv_done, drain;
+  uint64_t s_full[2], s_free[2], p_full[2], p_free[2], drain;
   uint32_t tmem_base;
   int abort;
+  int lim[kMaxCols];          // causal key limit of each query row of the tile
+  float red[4][kMaxCols];     // per-warp row maxima / row sums
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -74,15 +84,242 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+template <int NCOL>
+struct Cfg {
+  static constexpr uint32_t kPitch = NCOL * 2;                    // bytes of one P^T row (key)
+  static constexpr uint32_t kPBytes = kNt * kPitch;               // one P^T buffer
+  static constexpr uint32_t kPSwz = NCOL == 16 ? kSw32 : NCOL == 32 ? kSw64 : kSw128;
+  static constexpr uint32_t kTmemCols = NCOL == 16 ? 64 : NCOL == 32 ? 128 : 256;
+  // 16-byte chunk c of key row k as stored under the P^T swizzle
+  __device__ static __forceinline__ uint32_t pchunk(uint32_t c, uint32_t k) {
+    return NCOL == 16 ? (c ^ ((k >> 2) & 1u)) : NCOL == 32 ? (c ^ ((k >> 1) & 3u)) : (c ^ (k & 7u));
+  }
+};
+
+__host__ __device__ constexpr size_t gqa_fixed_bytes(int D, int ncol) {
+  return 1024 + (size_t)(D / 64) * ncol * 128 + 2 * (size_t)kNt * ncol * 2 + sizeof(Smem) + 64;
+}
+
+size_t gqa_stage_bytes(int D) { return 2 * (size_t)(D / 64) * kChunkBytes; }
+
+int gqa_stages(int D, int ncol) {
+  const size_t room = kSmemLimit - gqa_fixed_bytes(D, ncol);
+  const int s = (int)(room / gqa_stage_bytes(D));
+  return s > kMaxStages ? kMaxStages : s;
+}
+
+size_t gqa_smem_bytes(int D, int ncol, int stages) {
+  return gqa_fixed_bytes(D, ncol) + (size_t)stages * gqa_stage_bytes(D);
+}
+
+// Softmax and epilogue of the four softmax warps (thread = TMEM lane: key k of
+// the tile for S^T and P^T, value dim k for O^T).
+template <int NCOL, typename Fail>
+__device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, uint8_t* stages,
+                                                 uint32_t stage_bytes, uint8_t* ps, uint32_t tmem, int warp,
+                                                 int lane, int T, int kb, int ke, int lim_min, int R, int row0,
+                                                 int gsize, int g, int b, int r, int s_idx, Fail fail) {
+  using C = Cfg<NCOL>;
+  const int nch = p.D / 64;
+  const int qd = warp & 3;                                // TMEM lane quadrant of this warp
+  const int lrow = qd * 32 + lane;
+  const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
+  const uint32_t tO = lane_base + 2 * NCOL;
+  volatile int* abort_flag = &sm.abort;
+  float m[NCOL], l[NCOL];
+#pragma unroll
+  for (int h = 0; h < NCOL; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+  }
+  bool bad = false, broke = false;
+  for (int t = 0; t < T; ++t) {
+    const int bsel = t & 1;
+    const bool okw = __all_sync(0xffffffffu, *abort_flag == 0 &&
+                                                 mbar_wait(smem_u32(&sm.s_full[bsel]), (uint32_t)(t >> 1) & 1u, kWaitNs));
+    if (!okw) bad = true;
+    float x[NCOL];
+    {
+      uint32_t v[NCOL];
+      if (okw) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < NCOL / 16; ++c)
+          tmem_ld16(lane_base + bsel * NCOL + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&v[16 * c]));
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int h = 0; h < NCOL; ++h) v[h] = 0u;
+      }
+#pragma unroll
+      for (int h = 0; h < NCOL; ++h) x[h] = __uint_as_float(v[h]);
+    }
+    tc_fence_before();
+    mbar_arrive(smem_u32(&sm.s_free[bsel]));
+
+    // scaled scores (log2 domain); keys a row may not see are -inf
+    const int j0 = kb + t * kNt;
+    const int jj = j0 + lrow;                             // this thread's shard-local key
+    const bool full = j0 + kNt <= lim_min;                // every row sees every key of the tile
+    float e = -INFINITY;
+    if (full) {
+#pragma unroll
+      for (int h = 0; h < NCOL; ++h) {
+        x[h] *= p.scale_log2;
+        e = fmaxf(e, x[h] - m[h]);
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < NCOL; ++h) {
+        x[h] = jj < sm.lim[h] ? x[h] * p.scale_log2 : -INFINITY;
+        e = fmaxf(e, x[h] - m[h]);
+      }
+    }
+    // one barrier per tile: does any row's reference max have to move?
+    if (bar_red_or(kBarSoftmax, 128, e > kRescaleLog2 || bad)) {
+      if (bar_red_or(kBarSoftmax, 128, bad)) {
+        broke = true;
+        break;
+      }
+      // row maxima of the tile over its 128 keys
+#pragma unroll
+      for (int h = 0; h < NCOL; ++h) {
+        float v = x[h];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+        if (lane == 0) sm.red[qd][h] = v;
+      }
+      // O^T is rescaled below: the previous tile's PV must have landed.  Its
+      // P^T buffer's barrier is at most one phase ahead of what this thread
+      // last waited for there (PV(t-3)), so the parity is unambiguous.
+      if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_free[(t - 1) & 1]),
+                                                      (uint32_t)((t - 1) >> 1) & 1u, kWaitNs)))
+        bad = true;
+      if (bar_red_or(kBarSoftmax, 128, bad)) {
+        broke = true;
+        break;
+      }
+      float alpha[NCOL];
+#pragma unroll
+      for (int h = 0; h < NCOL; ++h) {
+        const float tmax = fmaxf(fmaxf(sm.red[0][h], sm.red[1][h]), fmaxf(sm.red[2][h], sm.red[3][h]));
+        const float mn = fmaxf(m[h], tmax);
+        alpha[h] = m[h] == -INFINITY ? 0.f : ex2(m[h] - mn);
+        m[h] = mn;
+        l[h] *= alpha[h];
+      }
+      if (t > 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < NCOL / 16; ++c) {
+          uint32_t o[16];
+          tmem_ld16(tO + 16 * c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha[16 * c + k]);
+          tmem_st16(tO + 16 * c, o);
+        }
+        tmem_wait_st();
+      }
+    }
+
+    // this key's probabilities for every row -> its P^T row (bf16)
+    uint32_t pk[NCOL / 2];
+    if (full) {
+#pragma unroll
+      for (int h = 0; h < NCOL; h += 2) {
+        const float p0 = ex2(x[h] - m[h]), p1 = ex2(x[h + 1] - m[h + 1]);
+        l[h] += p0;
+        l[h + 1] += p1;
+        pk[h / 2] = pack_bf16x2(p0, p1);
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < NCOL; h += 2) {
+        const float p0 = x[h] == -INFINITY ? 0.f : ex2(x[h] - m[h]);
+        const float p1 = x[h + 1] == -INFINITY ? 0.f : ex2(x[h + 1] - m[h + 1]);
+        l[h] += p0;
+        l[h + 1] += p1;
+        pk[h / 2] = pack_bf16x2(p0, p1);
+      }
+    }
+    if (t >= 2 &&
+        !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_free[bsel]), (uint32_t)((t >> 1) - 1) & 1u, kWaitNs)))
+      bad = true;
+    uint8_t* prow = ps + bsel * C::kPBytes + lrow * C::kPitch;
+#pragma unroll
+    for (int c = 0; c < NCOL / 8; ++c)
+      *reinterpret_cast<uint4*>(prow + (C::pchunk((uint32_t)c, (uint32_t)lrow) << 4)) =
+          make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    if (jj >= ke) {
+      // key past the range (ragged last tile): zero its value row so that
+      // 0 * (NaN/Inf) from a stale cache slot cannot reach O
+      uint8_t* vt = stages + (t % p.stages) * stage_bytes + lrow * 128;
+      for (int c = 0; c < nch; ++c) {
+        uint4* vr = reinterpret_cast<uint4*>(vt + c * kChunkBytes);
+#pragma unroll
+        for (int w = 0; w < 8; ++w) vr[w] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(smem_u32(&sm.p_full[bsel]));
+  }
+
+  // the last PV (its commit also covers every earlier MMA of the issuer)
+  bool have = T > 0 && !broke;
+  if (have && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_free[(T - 1) & 1]),
+                                                 (uint32_t)((T - 1) >> 1) & 1u, kWaitNs)))
+    bad = true;
+  if (bar_red_or(kBarSoftmax, 128, bad)) have = false;
+  if (bad) fail();
+
+  // row sums over the 128 key threads
+#pragma unroll
+  for (int h = 0; h < NCOL; ++h) {
+    float v = l[h];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) sm.red[qd][h] = v;
+  }
+  named_bar_sync(kBarSoftmax, 128);
+
+  // outputs: this thread holds value dim lrow of every row
+  uint32_t o[NCOL];
+#pragma unroll
+  for (int h = 0; h < NCOL; ++h) o[h] = 0u;
+  if (have) {
+    tc_fence_after();
+#pragma unroll
+    for (int c = 0; c < NCOL / 16; ++c) tmem_ld16(tO + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&o[16 * c]));
+    tmem_wait_ld();
+  }
+#pragma unroll
+  for (int h = 0; h < NCOL; ++h) {
+    if (h < R) {
+      const float lsum = (sm.red[0][h] + sm.red[1][h]) + (sm.red[2][h] + sm.red[3][h]);
+      const bool live = have && lsum > 0.f;
+      const int rr = row0 + h, i = rr / gsize, head = g * gsize + rr % gsize;
+      const long long urow = ((((long long)r * p.B + b) * p.Lq + i) * p.n_split + s_idx) * p.Hq + head;
+      if (lrow < p.D) p.dst_o[urow * p.D + lrow] = live ? __uint_as_float(o[h]) * (1.f / lsum) : 0.f;
+      if (lrow == 0) p.dst_lse[urow] = live ? (m[h] + log2f(lsum)) * 0.69314718055994531f : -INFINITY;
+    }
+  }
+}
+
+template <int NCOL>
 __global__ void __launch_bounds__(kThreads, 1)
 gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const GqaParams p) {
+  using C = Cfg<NCOL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int nch = p.D / 64;                               // 64-dim chunks of a row
-  const uint32_t stage_bytes = 2u * nch * kChunkBytes;    // K chunks, then V chunks
+  const uint32_t stage_bytes = 2u * nch * kChunkBytes;    // V chunks, then K chunks
   uint8_t* stages = base;
-  Smem& sm = *reinterpret_cast<Smem*>(base + p.stages * stage_bytes);
+  uint8_t* qs = stages + p.stages * stage_bytes;          // Q^T: nch chunks of NCOL rows x 128 B
+  uint8_t* ps = qs + nch * NCOL * 128;                    // two P^T buffers
+  Smem& sm = *reinterpret_cast<Smem*>(ps + 2 * C::kPBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long unit = blockIdx.x;
@@ -93,9 +330,8 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   const int b = (int)((gu / p.Hkv) % p.B);
   const int r = (int)(gu / ((long long)p.Hkv * p.B));
   const int gsize = p.Hq / p.Hkv;
-  const int row0 = 128 * mt;                              // first query row of this tile
-  const int R = min(128, p.Lq * gsize - row0);            // real query rows of this tile
-  const int n_act = (R + 31) / 32;                        // softmax warps holding real rows
+  const int row0 = NCOL * mt;                             // first query row of this tile
+  const int R = min(NCOL, p.Lq * gsize - row0);           // real query rows of this tile
 
   // key range: the tile's last query sees the most keys; earlier queries mask
   const int S = p.seq_lens[b];
@@ -103,11 +339,13 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   int L = bad_len ? 0 : local_len(S, r, p.I, p.N);
   const bool short_table = (long long)L > (long long)p.max_lb * p.bs;
   if (short_table) L = p.max_lb * p.bs;
-  const int i_last = (row0 + R - 1) / gsize;
+  const int i_first = row0 / gsize, i_last = (row0 + R - 1) / gsize;
   const int vis = bad_len ? 0 : min(L, local_count_upto((long long)S - p.Lq + i_last, r, p.I, p.N));
   const int kb = min(vis, s_idx * p.split_tokens);
   const int ke = min(vis, kb + p.split_tokens);
   const int T = (ke - kb + kNt - 1) / kNt;
+  // keys below lim_min are visible to every row of the tile
+  const int lim_min = bad_len ? 0 : min(ke, local_count_upto((long long)S - p.Lq + i_first, r, p.I, p.N));
   if (tid == 0 && (bad_len || short_table)) set_status(p.status, DCP_ERR_BOUNDS);
 
   if (tid == 0) {
@@ -115,46 +353,41 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       mbar_init(smem_u32(&sm.kv_full[k]), 1);
       mbar_init(smem_u32(&sm.kv_empty[k]), 1);
     }
-    mbar_init(smem_u32(&sm.s_full), 1);
-    mbar_init(smem_u32(&sm.s_free), 32 * n_act);
-    mbar_init(smem_u32(&sm.p_full), 32 * n_act);
-    mbar_init(smem_u32(&sm.pv_done), 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(smem_u32(&sm.s_full[k]), 1);
+      mbar_init(smem_u32(&sm.s_free[k]), 128);
+      mbar_init(smem_u32(&sm.p_full[k]), 128);
+      mbar_init(smem_u32(&sm.p_free[k]), 1);
+    }
     mbar_init(smem_u32(&sm.drain), 1);
     sm.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(&sm.tmem_base), 512);
+  if (warp == 1) tmem_alloc(smem_u32(&sm.tmem_base), C::kTmemCols);
+  if (warp >= 2) {
+    // Q^T rows -> smem, K-major with the 128-byte swizzle (rows >= R are zero),
+    // and the causal key limit of every row
+    const int st = tid - 64;
+    const int per_row = nch * 8;                          // 16-byte chunks of a row
+    for (int idx = st; idx < NCOL * per_row; idx += 128) {
+      const int h = idx / per_row, ch = (idx % per_row) >> 3, c = idx & 7;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (h < R && !bad_len) {
+        const int i = (row0 + h) / gsize, head = g * gsize + (row0 + h) % gsize;
+        v = __ldg(reinterpret_cast<const uint4*>(p.q + (((long long)b * p.Lq + i) * p.Hq + head) * p.D + ch * 64) + c);
+      }
+      *reinterpret_cast<uint4*>(qs + ch * NCOL * 128 + h * 128 + ((c ^ (h & 7)) << 4)) = v;
+    }
+    if (st < NCOL) {
+      sm.lim[st] = (st < R && !bad_len)
+                       ? min(ke, local_count_upto((long long)S - p.Lq + (row0 + st) / gsize, r, p.I, p.N))
+                       : ke;
+    }
+    fence_proxy_async_smem();
+  }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-
-  // query rows -> TMEM (row = TMEM lane; rows >= R are zero)
-  if (warp >= 2) {
-    const int row = (warp & 3) * 32 + lane;
-    const uint32_t lane_addr = taddr(tmem, (uint32_t)((warp & 3) * 32), 0);
-    const bool real = row < R && !bad_len;
-    const uint4* qrow = nullptr;
-    if (real) {
-      const int i = (row0 + row) / gsize, head = g * gsize + (row0 + row) % gsize;
-      qrow = reinterpret_cast<const uint4*>(p.q + (((long long)b * p.Lq + i) * p.Hq + head) * p.D);
-    }
-    for (int c = 0; c < p.D / 32; ++c) {                  // 16 columns = 32 dims per store
-      uint32_t v[16];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint4 w = real ? __ldg(qrow + 4 * c + k) : make_uint4(0u, 0u, 0u, 0u);
-        v[4 * k + 0] = w.x;
-        v[4 * k + 1] = w.y;
-        v[4 * k + 2] = w.z;
-        v[4 * k + 3] = w.w;
-      }
-      tmem_st16(lane_addr + kColQ + 16 * c, v);
-    }
-    tmem_wait_st();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
 
   volatile int* abort_flag = &sm.abort;
   auto fail = [&](void) {
@@ -191,8 +424,8 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
           if ((unsigned)blk >= (unsigned)p.num_blocks) set_status(p.status, DCP_ERR_BOUNDS);
           const int row = blk * p.bs + (j % p.bs);       // out-of-range rows read as zeros
           for (int c = 0; c < nch; ++c) {
-            tma_load_3d(smem_u32(dst + c * kChunkBytes + k * box_rows * 128), &tm_k, 64 * c, g, row, full);
-            tma_load_3d(smem_u32(dst + (nch + c) * kChunkBytes + k * box_rows * 128), &tm_v, 64 * c, g, row,
+            tma_load_3d(smem_u32(dst + c * kChunkBytes + k * box_rows * 128), &tm_v, 64 * c, g, row, full);
+            tma_load_3d(smem_u32(dst + (nch + c) * kChunkBytes + k * box_rows * 128), &tm_k, 64 * c, g, row,
                         full);
           }
         }
@@ -206,18 +439,22 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0 && T > 0) {
-      const uint32_t id_qk = idesc_bf16(128, kNt, false);
-      const uint32_t id_pv = idesc_bf16(128, p.D, true);
+      constexpr uint32_t id_qk = idesc_bf16_ab(128, NCOL, false, false);
+      constexpr uint32_t id_pv = idesc_bf16_ab(128, NCOL, true, true);
+      const uint32_t tO = tmem + 2 * NCOL;
       auto issue_pv = [&](int t) -> bool {
-        if (*abort_flag || !mbar_wait(smem_u32(&sm.p_full), (uint32_t)t & 1u, kWaitNs)) return false;
+        if (*abort_flag || !mbar_wait(smem_u32(&sm.p_full[t & 1]), (uint32_t)(t >> 1) & 1u, kWaitNs)) return false;
         tc_fence_after();
-        const uint8_t* vb = stages + (t % p.stages) * stage_bytes + nch * kChunkBytes;
+        const uint8_t* vb = stages + (t % p.stages) * stage_bytes;
+        const uint8_t* pb = ps + (t & 1) * C::kPBytes;
 #pragma unroll
         for (int k = 0; k < kNt / 16; ++k) {
-          const uint64_t bdesc = smem_desc(smem_u32(vb + k * 2048), kChunkBytes, 1024, kSw128);
-          mma_ts(tmem + kColO, tmem + kColP + 8 * k, bdesc, id_pv, (t > 0 || k > 0) ? 1u : 0u);
+          // A = V^T (dims x keys) read MN-major from the value chunks; B = P^T
+          const uint64_t adesc = smem_desc(smem_u32(vb + k * 2048), kChunkBytes, 1024, kSw128);
+          const uint64_t bdesc = smem_desc(smem_u32(pb + k * 16 * C::kPitch), C::kPBytes, 8 * C::kPitch, C::kPSwz);
+          mma_ss(tO, adesc, bdesc, id_pv, (t > 0 || k > 0) ? 1u : 0u);
         }
-        mma_commit(smem_u32(&sm.pv_done));
+        mma_commit(smem_u32(&sm.p_free[t & 1]));
         mma_commit(smem_u32(&sm.kv_empty[t % p.stages]));
         return true;
       };
@@ -226,17 +463,18 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         const int st = t % p.stages;
         if (*abort_flag ||
             !mbar_wait(smem_u32(&sm.kv_full[st]), (uint32_t)(t / p.stages) & 1u, kWaitNs) ||
-            (t > 0 && !mbar_wait(smem_u32(&sm.s_free), (uint32_t)(t - 1) & 1u, kWaitNs))) {
+            (t >= 2 && !mbar_wait(smem_u32(&sm.s_free[t & 1]), (uint32_t)((t >> 1) - 1) & 1u, kWaitNs))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint8_t* kbuf = stages + st * stage_bytes;
+        const uint8_t* kbuf = stages + st * stage_bytes + nch * kChunkBytes;
         for (int k = 0; k < p.D / 16; ++k) {
-          const uint64_t bdesc = smem_desc(smem_u32(kbuf + (k >> 2) * kChunkBytes + (k & 3) * 32), 16, 1024, kSw128);
-          mma_ts(tmem + kColS, tmem + kColQ + 8 * k, bdesc, id_qk, k > 0 ? 1u : 0u);
+          const uint64_t adesc = smem_desc(smem_u32(kbuf + (k >> 2) * kChunkBytes + (k & 3) * 32), 16, 1024, kSw128);
+          const uint64_t bdesc = smem_desc(smem_u32(qs + (k >> 2) * (NCOL * 128) + (k & 3) * 32), 16, 1024, kSw128);
+          mma_ss(tmem + (t & 1) * NCOL, adesc, bdesc, id_qk, k > 0 ? 1u : 0u);
         }
-        mma_commit(smem_u32(&sm.s_full));
+        mma_commit(smem_u32(&sm.s_full[t & 1]));
         if (t > 0) ok = issue_pv(t - 1);
       }
       if (ok) ok = issue_pv(T - 1);
@@ -244,135 +482,27 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       mma_commit(smem_u32(&sm.drain));
       if (!mbar_wait(smem_u32(&sm.drain), 0, kWaitNs)) fail();
     }
-  } else if ((warp & 3) < n_act) {
-    // ---------------- softmax / epilogue (warps holding real rows) ----------------
-    const int lg = warp & 3;
-    const int row = lg * 32 + lane;
-    const bool real = row < R;
-    const int i_q = real ? (row0 + row) / gsize : 0;
-    const int head = g * gsize + (real ? (row0 + row) % gsize : 0);
-    const uint32_t lane_addr = taddr(tmem, (uint32_t)(lg * 32), 0);
-    // causal limit of this row's query: a prefix of the shard-local keys
-    const int lim = real ? min(ke, local_count_upto((long long)S - p.Lq + i_q, r, p.I, p.N)) : kb;
-    float m_ref = -INFINITY, l = 0.f;
-    bool ok = true;
-    auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
-      if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
-      return __all_sync(0xffffffffu, mbar_wait(bar, par, kWaitNs));
-    };
-    for (int t = 0; t < T; ++t) {
-      if (!wwait(smem_u32(&sm.s_full), (uint32_t)t & 1u)) { ok = false; break; }
-      tc_fence_after();
-      float x[kNt];
-      {
-        uint32_t v[32];
-        tmem_ld32(lane_addr + kColS, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(v[k]);
-        tmem_ld32(lane_addr + kColS + 32, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 32; ++k) x[32 + k] = __uint_as_float(v[k]);
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.s_free));
-      const int j0 = kb + t * kNt;
-      const int valid = min(kNt, lim - j0);               // may be <= 0 for early queries
-      float tmax = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < kNt; ++k) {
-        x[k] = (k < valid) ? x[k] * p.scale_log2 : -INFINITY;
-        tmax = fmaxf(tmax, x[k]);
-      }
-      const bool grow = tmax > m_ref + kRescaleLog2;
-      float alpha = 1.f;
-      if (grow) {
-        alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - tmax);
-        m_ref = tmax;
-      }
-      l *= alpha;
-      uint32_t pk[kNt / 2];
-#pragma unroll
-      for (int k = 0; k < kNt; k += 2) {
-        const float p0 = (k < valid) ? ex2(x[k] - m_ref) : 0.f;
-        const float p1 = (k + 1 < valid) ? ex2(x[k + 1] - m_ref) : 0.f;
-        l += p0 + p1;
-        pk[k / 2] = pack_bf16x2(p0, p1);
-      }
-      if (t > 0) {
-        if (!wwait(smem_u32(&sm.pv_done), (uint32_t)(t - 1) & 1u)) { ok = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, grow)) {
-          for (int c = 0; c < p.D; c += 32) {
-            uint32_t v[32];
-            tmem_ld32(lane_addr + kColO + c, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-            tmem_st32(lane_addr + kColO + c, v);
-          }
-        }
-      }
-      const int tile_valid = min(kNt, ke - j0);
-      if (tile_valid < kNt) {
-        // ragged last tile: zero the value rows past the sequence end so that
-        // 0 * (NaN/Inf) from stale cache slots cannot reach O
-        uint4* vt = reinterpret_cast<uint4*>(stages + (t % p.stages) * stage_bytes + nch * kChunkBytes);
-        const int n16 = (kNt - tile_valid) * 8;
-        for (int idx = row; idx < nch * n16; idx += 32 * n_act) {   // row: 0 .. 32*n_act-1
-          const int c = idx / n16, w = idx % n16;
-          vt[(c * kChunkBytes) / 16 + tile_valid * 8 + w] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
-      }
-      tmem_st32(lane_addr + kColP, pk);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.p_full));
-    }
-    if (!ok) fail();
-    bool have = ok && T > 0;
-    if (have) {
-      have = wwait(smem_u32(&sm.pv_done), (uint32_t)(T - 1) & 1u);
-      if (!have) fail();
-    }
-    tc_fence_after();
-    const long long urow =
-        ((((long long)r * p.B + b) * p.Lq + i_q) * p.n_split + s_idx) * p.Hq + head;
-    float* orow = p.dst_o + urow * p.D;
-    if (have) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      for (int c = 0; c < p.D; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(lane_addr + kColO + c, v);             // whole warp: .sync.aligned
-        tmem_wait_ld();
-        if (real) {
-          float4* dst = reinterpret_cast<float4*>(orow + c);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
-                                 __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
-        }
-      }
-      if (real) p.dst_lse[urow] = l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
-    } else if (real) {
-      float4* dst = reinterpret_cast<float4*>(orow);
-      for (int k = 0; k < p.D / 4; ++k) dst[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      p.dst_lse[urow] = -INFINITY;
-    }
+  } else {
+    softmax_epilogue<NCOL>(p, sm, stages, stage_bytes, ps, tmem, warp, lane, T, kb, ke, lim_min, R, row0,
+                           gsize, g, b, r, s_idx, fail);
   }
 
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
-size_t gqa_smem_bytes(int D, int stages) {
-  return 1024 + (size_t)stages * 2 * (D / 64) * kChunkBytes + sizeof(Smem) + 64;
+template <int NCOL>
+cudaError_t launch_ncol(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const GqaParams& p, long long units,
+                        cudaStream_t stream) {
+  const size_t smem = gqa_smem_bytes(p.D, NCOL, p.stages);
+  cudaError_t e = cudaFuncSetAttribute(gqa_attn_kernel<NCOL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  gqa_attn_kernel<NCOL><<<(unsigned)units, kThreads, smem, stream>>>(tm_k, tm_v, p);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -385,7 +515,17 @@ bool gqa_tc_supported(const AttnArgs& a) {
   return (long long)a.num_blocks * a.bs < (1LL << 31);
 }
 
-static int gqa_m_tiles(const AttnArgs& a) { return (int)(((long long)a.Lq * (a.Hq / a.Hkv) + 127) / 128); }
+// Query rows per row tile: the group's rows of all queries, padded to 16, 32
+// or 64; more rows than 64 take several tiles.
+static int gqa_ncol(const AttnArgs& a) {
+  const long long rows = (long long)a.Lq * (a.Hq / a.Hkv);
+  return rows <= 16 ? 16 : rows <= 32 ? 32 : kMaxCols;
+}
+
+static int gqa_m_tiles(const AttnArgs& a) {
+  const long long rows = (long long)a.Lq * (a.Hq / a.Hkv);
+  return (int)((rows + gqa_ncol(a) - 1) / gqa_ncol(a));
+}
 
 SplitPlan plan_attn_gqa_tc(const AttnArgs& a, int sm_count) {
   return plan_splits(a, sm_count, kNt, a.Hkv * gqa_m_tiles(a));
@@ -402,6 +542,7 @@ cudaError_t launch_attn_gqa_tc(const AttnArgs& a, const SplitPlan& plan) {
   if (!make_tensor_map_bf16(&tm_k, k_pool, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tensor_map_bf16(&tm_v, v_pool, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  const int ncol = gqa_ncol(a);
   GqaParams p;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.block_tables = a.block_tables;
@@ -420,7 +561,7 @@ cudaError_t launch_attn_gqa_tc(const AttnArgs& a, const SplitPlan& plan) {
   p.split_tokens = plan.split_tokens;
   p.m_tiles = gqa_m_tiles(a);
   p.D = a.Dqk;
-  p.stages = kMaxStages;
+  p.stages = gqa_stages(a.Dqk, ncol);
   p.scale_log2 = a.scale * 1.4426950408889634f;
   if (plan.n_split > 1) {
     const size_t nrows = (size_t)a.N * a.B * a.Lq * a.Hq;
@@ -431,13 +572,11 @@ cudaError_t launch_attn_gqa_tc(const AttnArgs& a, const SplitPlan& plan) {
     p.dst_o = a.partial_out;
     p.dst_lse = a.lse;
   }
-  const size_t smem = gqa_smem_bytes(p.D, p.stages);
-  cudaError_t e = cudaFuncSetAttribute(gqa_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   const long long units = (long long)a.N * a.B * a.Hkv * p.m_tiles * plan.n_split;
   if (units == 0) return cudaSuccess;
-  gqa_attn_kernel<<<(unsigned)units, kThreads, smem, a.stream>>>(tm_k, tm_v, p);
-  e = cudaGetLastError();
+  cudaError_t e = ncol == 16   ? launch_ncol<16>(tm_k, tm_v, p, units, a.stream)
+                  : ncol == 32 ? launch_ncol<32>(tm_k, tm_v, p, units, a.stream)
+                               : launch_ncol<kMaxCols>(tm_k, tm_v, p, units, a.stream);
   if (e != cudaSuccess || plan.n_split <= 1) return e;
   return launch_split_combine(a, plan);
 }

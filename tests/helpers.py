@@ -91,3 +91,34 @@ def repage(inst: wl.Instance, w2: wl.Workload) -> wl.Instance:
                 kv[blk, off] = torch.from_numpy(Ks[b][toks][:, 0]).to(kv.dtype)
     new.q.copy_(inst.q.cpu())
     return new
+
+
+
+def scale_keys_by_position(inst: wl.Instance, factor, value_scale: float = 1.0,
+                           key_dims: slice = slice(None)) -> wl.Instance:
+    """Multiply the dims ``key_dims`` of every cached key row at global position
+    t of a request of length S by factor(t / S), and every value row by
+    ``value_scale``, in place (MLA: scale only the rope dims to leave the
+    values alone).  Scores that grow along the sequence move the running
+    reference max many times, tile after tile."""
+    w = inst.w
+    kv = inst.kv_cache
+    bt = inst.block_tables.numpy()
+    for b, S in enumerate(inst.seq_lens.tolist()):
+        for r, toks in enumerate(orc.shard_token_lists(S, w.interleave, w.dcp_size)):
+            if not len(toks):
+                continue
+            j = np.arange(len(toks))
+            blk = torch.from_numpy(bt[r][b][j // w.block_size].astype(np.int64))
+            off = torch.from_numpy(j % w.block_size)
+            f = torch.as_tensor(factor(np.asarray(toks, dtype=np.float64) / S))
+            if w.kind == "gqa":
+                rows = kv[0][blk, off].double()
+                rows[..., key_dims] *= f.view(-1, 1, 1)
+                kv[0][blk, off] = rows.to(kv.dtype)
+                kv[1][blk, off] = (kv[1][blk, off].double() * value_scale).to(kv.dtype)
+            else:
+                rows = kv[blk, off].double()
+                rows[..., key_dims] *= f.view(-1, 1)
+                kv[blk, off] = rows.to(kv.dtype)
+    return inst

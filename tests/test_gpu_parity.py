@@ -108,6 +108,37 @@ def test_attention_matches_oracle(name, kw):
     check_against_oracle(inst)
 
 
+GROWING_CASES = [
+    ("qwen_gqa", dict(batch=2, lengths=("uniform", 1500, 4000), dcp_size=2)),
+    ("qwen_gqa", dict(batch=1, q_len=4, lengths=("fixed", 3000), dcp_size=2, interleave=64)),
+    ("tiny_gqa", dict(batch=2, lengths=("uniform", 700, 1500), dcp_size=2, interleave=16)),
+    ("mla_32", dict(batch=2, lengths=("uniform", 2000, 5000), dcp_size=4)),
+]
+
+
+@pytest.mark.parametrize("name,kw", GROWING_CASES)
+def test_attention_with_scores_growing_along_the_sequence(name, kw):
+    """GQA keys scaled up to 8x (16x in a spike near the end): each row's running
+    max moves past its lazy-rescale threshold in later tiles, not only the first.
+
+    Such peaked softmaxes put the bf16 rounding of the probabilities (2^-9
+    relative, before the PV product) at up to 2^-9 * max|v| in the output, so
+    the GQA values are scaled by 1/4 to keep that inside the 2e-3 bound; MLA
+    grows only its 64 rope dims (up to 16x, no spike), which leaves the values
+    (the latent) alone.
+    A wrong rescale errs by the size of the output itself."""
+    inst = H.build_instance(H.small(name, **kw))
+
+    def factor(u):
+        return np.where(u > 0.97, 16.0, 1.0 + 7.0 * u * u)
+
+    if inst.w.kind == "gqa":
+        H.scale_keys_by_position(inst, factor, value_scale=0.25)
+    else:
+        H.scale_keys_by_position(inst, lambda u: 1.0 + 15.0 * u * u, key_dims=slice(inst.w.head_dim_v, None))
+    check_against_oracle(inst)
+
+
 @pytest.mark.parametrize("N", [1, 2, 4, 8])
 def test_mtp_merge_invariance_sweep(N):
     """MTP verify (Lq 4, interleave 1): merged output equals the oracle at every dcp_size."""
