@@ -5,7 +5,8 @@
 // section "Grouped-Query Attention (GQA) 後端" (query heads grouped over a few
 // KV heads; query head h reads KV head h / (Hq / Hkv)).
 //
-// Work unit = (shard r, request b, KV head g, row tile m, KV split s), one CTA.
+// Work unit = (shard r, request b, KV head g, row tile m, KV split s), one CTA;
+// units run longest request first (batches up to 128).
 // The query rows of KV head g - (query i, head of the group), Lq * Hq / Hkv of
 // them - are few (16 for one decode token of a 16-head group), so the kernel
 // computes the transposed products and puts the KEYS on the 128 rows of the
@@ -27,8 +28,12 @@
 // the tile's row maxima, rescale O^T (after the previous PV has landed) and
 // their per-thread row sums.  Row sums are reduced across the 128 key threads
 // once, at the end.  Logs are base 2 with the scale folded into the exponent.
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner, warps 2..5 softmax/epilogue.  Every wait is bounded; on expiry the
+// Warp roles (224 threads): warp 0 TMA producer, warp 1 QK issuer and TMEM
+// owner, warp 2 PV issuer, warps 3..6 softmax/epilogue.  A tcgen05.mma takes
+// one issuing thread tens of cycles, so QK and PV have a thread each (PV(t)
+// goes out as soon as P(t) is ready, not after the next tile's QK) and every
+// shared-memory descriptor is a precomputed base plus a constant offset.
+// Every wait is bounded; on expiry the
 // kernel records DCP_ERR_TIMEOUT and unwinds, the softmax warps deciding
 // together (barrier-reduced predicates) so that none is left at a barrier.
 #include <cuda.h>
@@ -47,12 +52,13 @@ using namespace sm100;
 constexpr int kNt = 128;                       // keys per tile (MMA M of S^T)
 constexpr int kMaxStages = 6;
 constexpr uint32_t kChunkBytes = kNt * 128;    // 128 keys x 64 dims bf16
-constexpr uint32_t kThreads = 192;
+constexpr uint32_t kThreads = 224;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxCols = 64;                   // query rows per row tile
 constexpr size_t kSmemLimit = 232448;          // dynamic shared memory per CTA
 constexpr uint32_t kBarSoftmax = 1;            // named barrier of the softmax warps
+constexpr int kLptMaxBatch = 128;              // longest-first unit order up to this batch
 
 struct GqaParams {
   const __nv_bfloat16* q;
@@ -71,9 +77,10 @@ struct GqaParams {
 struct Smem {
   uint64_t kv_full[kMaxStages];
   uint64_t kv_empty[kMaxStages];
-  uint64_t s_full[2], s_free[2], p_full[2], p_free[2], drain;
+  uint64_t s_full[2], s_free[2], p_full[2], p_free[2], drain[2];
   uint32_t tmem_base;
   int abort;
+  int req;                    // request of this unit
   int lim[kMaxCols];          // causal key limit of each query row of the tile
   float red[4][kMaxCols];     // per-warp row maxima / row sums
 };
@@ -322,13 +329,31 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   Smem& sm = *reinterpret_cast<Smem*>(ps + 2 * C::kPBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Units in longest-request-first order: the block scheduler starts CTAs in
+  // index order, so the short units fill the tail.  Rank k of the request
+  // order (length descending, index ascending) is found by counting.
   const long long unit = blockIdx.x;
-  const int s_idx = (int)(unit % p.n_split);
-  const int mt = (int)((unit / p.n_split) % p.m_tiles);
-  const long long gu = unit / ((long long)p.n_split * p.m_tiles);
-  const int g = (int)(gu % p.Hkv);
-  const int b = (int)((gu / p.Hkv) % p.B);
-  const int r = (int)(gu / ((long long)p.Hkv * p.B));
+  const long long per_req = (long long)p.N * p.Hkv * p.m_tiles * p.n_split;
+  const int k_req = (int)(unit / per_req);
+  int b = k_req;
+  if (p.B <= kLptMaxBatch) {
+    for (int j = tid; j < p.B; j += kThreads) {
+      const int sj = p.seq_lens[j];
+      int rank = 0;
+      for (int i = 0; i < p.B; ++i) {
+        const int si = p.seq_lens[i];
+        rank += (si > sj) || (si == sj && i < j);
+      }
+      if (rank == k_req) sm.req = j;
+    }
+    __syncthreads();
+    b = sm.req;
+  }
+  const long long rest = unit % per_req;
+  const int s_idx = (int)(rest % p.n_split);
+  const int mt = (int)((rest / p.n_split) % p.m_tiles);
+  const int g = (int)((rest / ((long long)p.n_split * p.m_tiles)) % p.Hkv);
+  const int r = (int)(rest / ((long long)p.n_split * p.m_tiles * p.Hkv));
   const int gsize = p.Hq / p.Hkv;
   const int row0 = NCOL * mt;                             // first query row of this tile
   const int R = min(NCOL, p.Lq * gsize - row0);           // real query rows of this tile
@@ -359,15 +384,16 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       mbar_init(smem_u32(&sm.p_full[k]), 128);
       mbar_init(smem_u32(&sm.p_free[k]), 1);
     }
-    mbar_init(smem_u32(&sm.drain), 1);
+    mbar_init(smem_u32(&sm.drain[0]), 1);
+    mbar_init(smem_u32(&sm.drain[1]), 1);
     sm.abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(&sm.tmem_base), C::kTmemCols);
-  if (warp >= 2) {
+  if (warp >= 3) {
     // Q^T rows -> smem, K-major with the 128-byte swizzle (rows >= R are zero),
     // and the causal key limit of every row
-    const int st = tid - 64;
+    const int st = tid - 96;
     const int per_row = nch * 8;                          // 16-byte chunks of a row
     for (int idx = st; idx < NCOL * per_row; idx += 128) {
       const int h = idx / per_row, ch = (idx % per_row) >> 3, c = idx & 7;
@@ -437,29 +463,20 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+    // ---------------- QK issuer: S^T(t) = K(t) Q^T ----------------
     if (lane == 0 && T > 0) {
       constexpr uint32_t id_qk = idesc_bf16_ab(128, NCOL, false, false);
-      constexpr uint32_t id_pv = idesc_bf16_ab(128, NCOL, true, true);
-      const uint32_t tO = tmem + 2 * NCOL;
-      auto issue_pv = [&](int t) -> bool {
-        if (*abort_flag || !mbar_wait(smem_u32(&sm.p_full[t & 1]), (uint32_t)(t >> 1) & 1u, kWaitNs)) return false;
-        tc_fence_after();
-        const uint8_t* vb = stages + (t % p.stages) * stage_bytes;
-        const uint8_t* pb = ps + (t & 1) * C::kPBytes;
-#pragma unroll
-        for (int k = 0; k < kNt / 16; ++k) {
-          // A = V^T (dims x keys) read MN-major from the value chunks; B = P^T
-          const uint64_t adesc = smem_desc(smem_u32(vb + k * 2048), kChunkBytes, 1024, kSw128);
-          const uint64_t bdesc = smem_desc(smem_u32(pb + k * 16 * C::kPitch), C::kPBytes, 8 * C::kPitch, C::kPSwz);
-          mma_ss(tO, adesc, bdesc, id_pv, (t > 0 || k > 0) ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&sm.p_free[t & 1]));
-        mma_commit(smem_u32(&sm.kv_empty[t % p.stages]));
-        return true;
-      };
+      // descriptor start addresses are 16-byte units in the low bits: a byte
+      // offset inside shared memory is added as offset >> 4.  The K-step loops
+      // stay rolled, offsets computed at run time: fully unrolled runs of MMAs
+      // whose descriptors were a base plus compile-time offsets inside a
+      // swizzle row gave wrong products on the device (the same values
+      // computed per step did not)
+      const uint64_t dk0 = smem_desc(smem_u32(stages + nch * kChunkBytes), 16, 1024, kSw128);
+      const uint64_t dq0 = smem_desc(smem_u32(qs), 16, 1024, kSw128);
+      const uint32_t ksteps = (uint32_t)p.D / 16;
       bool ok = true;
-      for (int t = 0; t < T && ok; ++t) {
+      for (int t = 0; t < T; ++t) {
         const int st = t % p.stages;
         if (*abort_flag ||
             !mbar_wait(smem_u32(&sm.kv_full[st]), (uint32_t)(t / p.stages) & 1u, kWaitNs) ||
@@ -468,19 +485,47 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
           break;
         }
         tc_fence_after();
-        const uint8_t* kbuf = stages + st * stage_bytes + nch * kChunkBytes;
-        for (int k = 0; k < p.D / 16; ++k) {
-          const uint64_t adesc = smem_desc(smem_u32(kbuf + (k >> 2) * kChunkBytes + (k & 3) * 32), 16, 1024, kSw128);
-          const uint64_t bdesc = smem_desc(smem_u32(qs + (k >> 2) * (NCOL * 128) + (k & 3) * 32), 16, 1024, kSw128);
-          mma_ss(tmem + (t & 1) * NCOL, adesc, bdesc, id_qk, k > 0 ? 1u : 0u);
+        const uint64_t dk = dk0 + ((uint64_t)(st * stage_bytes) >> 4);
+        const uint32_t dS = tmem + (uint32_t)(t & 1) * NCOL;
+#pragma unroll 1
+        for (uint32_t k = 0; k < ksteps; ++k) {
+          const uint64_t off = (uint64_t)(((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4);
+          const uint64_t offq = (uint64_t)(((k >> 2) * NCOL * 128 + (k & 3) * 32) >> 4);
+          mma_ss(dS, dk + off, dq0 + offq, id_qk, k > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(&sm.s_full[t & 1]));
-        if (t > 0) ok = issue_pv(t - 1);
       }
-      if (ok) ok = issue_pv(T - 1);
       if (!ok) fail();
-      mma_commit(smem_u32(&sm.drain));
-      if (!mbar_wait(smem_u32(&sm.drain), 0, kWaitNs)) fail();
+      mma_commit(smem_u32(&sm.drain[0]));
+      if (!mbar_wait(smem_u32(&sm.drain[0]), 0, kWaitNs)) fail();
+    }
+  } else if (warp == 2) {
+    // ---------------- PV issuer: O^T += V^T(t) P^T(t) ----------------
+    if (lane == 0 && T > 0) {
+      constexpr uint32_t id_pv = idesc_bf16_ab(128, NCOL, true, true);
+      const uint32_t tO = tmem + 2 * NCOL;
+      // A = V^T (dims x keys) read MN-major from the value chunks; B = P^T
+      const uint64_t dv0 = smem_desc(smem_u32(stages), kChunkBytes, 1024, kSw128);
+      const uint64_t dp0 = smem_desc(smem_u32(ps), C::kPBytes, 8 * C::kPitch, C::kPSwz);
+      bool ok = true;
+      for (int t = 0; t < T; ++t) {
+        if (*abort_flag || !mbar_wait(smem_u32(&sm.p_full[t & 1]), (uint32_t)(t >> 1) & 1u, kWaitNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int st = t % p.stages;
+        const uint64_t dv = dv0 + ((uint64_t)(st * stage_bytes) >> 4);
+        const uint64_t dp = dp0 + ((uint64_t)((t & 1) * C::kPBytes) >> 4);
+#pragma unroll 1
+        for (uint32_t k = 0; k < kNt / 16; ++k)
+          mma_ss(tO, dv + ((k * 2048u) >> 4), dp + ((k * 16u * C::kPitch) >> 4), id_pv, (t > 0 || k > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&sm.p_free[t & 1]));
+        mma_commit(smem_u32(&sm.kv_empty[st]));
+      }
+      if (!ok) fail();
+      mma_commit(smem_u32(&sm.drain[1]));
+      if (!mbar_wait(smem_u32(&sm.drain[1]), 0, kWaitNs)) fail();
     }
   } else {
     softmax_epilogue<NCOL>(p, sm, stages, stage_bytes, ps, tmem, warp, lane, T, kb, ke, lim_min, R, row0,
