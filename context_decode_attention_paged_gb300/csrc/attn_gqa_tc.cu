@@ -31,8 +31,7 @@
 // Warp roles (224 threads): warp 0 TMA producer, warp 1 QK issuer and TMEM
 // owner, warp 2 PV issuer, warps 3..6 softmax/epilogue.  A tcgen05.mma takes
 // one issuing thread tens of cycles, so QK and PV have a thread each (PV(t)
-// goes out as soon as P(t) is ready, not after the next tile's QK) and every
-// shared-memory descriptor is a precomputed base plus a constant offset.
+// goes out as soon as P(t) is ready, not after the next tile's QK).
 // Every wait is bounded; on expiry the
 // kernel records DCP_ERR_TIMEOUT and unwinds, the softmax warps deciding
 // together (barrier-reduced predicates) so that none is left at a barrier.
@@ -466,14 +465,10 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     // ---------------- QK issuer: S^T(t) = K(t) Q^T ----------------
     if (lane == 0 && T > 0) {
       constexpr uint32_t id_qk = idesc_bf16_ab(128, NCOL, false, false);
-      // descriptor start addresses are 16-byte units in the low bits: a byte
-      // offset inside shared memory is added as offset >> 4.  The K-step loops
-      // stay rolled, offsets computed at run time: fully unrolled runs of MMAs
-      // whose descriptors were a base plus compile-time offsets inside a
-      // swizzle row gave wrong products on the device (the same values
-      // computed per step did not)
-      const uint64_t dk0 = smem_desc(smem_u32(stages + nch * kChunkBytes), 16, 1024, kSw128);
-      const uint64_t dq0 = smem_desc(smem_u32(qs), 16, 1024, kSw128);
+      // Each descriptor is built from its address at the MMA, in an unrolled
+      // K-step loop.  (A variant that added compile-time offsets inside a
+      // swizzle row to a 64-bit base descriptor gave wrong products on the
+      // device, although the descriptor values it printed were the same.)
       const uint32_t ksteps = (uint32_t)p.D / 16;
       bool ok = true;
       for (int t = 0; t < T; ++t) {
@@ -485,13 +480,14 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
           break;
         }
         tc_fence_after();
-        const uint64_t dk = dk0 + ((uint64_t)(st * stage_bytes) >> 4);
         const uint32_t dS = tmem + (uint32_t)(t & 1) * NCOL;
-#pragma unroll 1
-        for (uint32_t k = 0; k < ksteps; ++k) {
-          const uint64_t off = (uint64_t)(((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4);
-          const uint64_t offq = (uint64_t)(((k >> 2) * NCOL * 128 + (k & 3) * 32) >> 4);
-          mma_ss(dS, dk + off, dq0 + offq, id_qk, k > 0 ? 1u : 0u);
+        const uint8_t* kbuf = stages + st * stage_bytes + nch * kChunkBytes;
+#pragma unroll
+        for (uint32_t k = 0; k < 8; ++k) {
+          if (k < ksteps)
+            mma_ss(dS, smem_desc(smem_u32(kbuf + (k >> 2) * kChunkBytes + (k & 3) * 32), 16, 1024, kSw128),
+                   smem_desc(smem_u32(qs + (k >> 2) * (NCOL * 128) + (k & 3) * 32), 16, 1024, kSw128), id_qk,
+                   k > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(&sm.s_full[t & 1]));
       }
@@ -505,8 +501,6 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       constexpr uint32_t id_pv = idesc_bf16_ab(128, NCOL, true, true);
       const uint32_t tO = tmem + 2 * NCOL;
       // A = V^T (dims x keys) read MN-major from the value chunks; B = P^T
-      const uint64_t dv0 = smem_desc(smem_u32(stages), kChunkBytes, 1024, kSw128);
-      const uint64_t dp0 = smem_desc(smem_u32(ps), C::kPBytes, 8 * C::kPitch, C::kPSwz);
       bool ok = true;
       for (int t = 0; t < T; ++t) {
         if (*abort_flag || !mbar_wait(smem_u32(&sm.p_full[t & 1]), (uint32_t)(t >> 1) & 1u, kWaitNs)) {
@@ -515,11 +509,11 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         }
         tc_fence_after();
         const int st = t % p.stages;
-        const uint64_t dv = dv0 + ((uint64_t)(st * stage_bytes) >> 4);
-        const uint64_t dp = dp0 + ((uint64_t)((t & 1) * C::kPBytes) >> 4);
-#pragma unroll 1
+#pragma unroll
         for (uint32_t k = 0; k < kNt / 16; ++k)
-          mma_ss(tO, dv + ((k * 2048u) >> 4), dp + ((k * 16u * C::kPitch) >> 4), id_pv, (t > 0 || k > 0) ? 1u : 0u);
+          mma_ss(tO, smem_desc(smem_u32(stages + st * stage_bytes + k * 2048), kChunkBytes, 1024, kSw128),
+                 smem_desc(smem_u32(ps + (t & 1) * C::kPBytes + k * 16 * C::kPitch), C::kPBytes, 8 * C::kPitch, C::kPSwz),
+                 id_pv, (t > 0 || k > 0) ? 1u : 0u);
         mma_commit(smem_u32(&sm.p_free[t & 1]));
         mma_commit(smem_u32(&sm.kv_empty[st]));
       }
