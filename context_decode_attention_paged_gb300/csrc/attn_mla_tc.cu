@@ -7,7 +7,8 @@
 // section "Multi-head Latent Attention (MLA) 後端" (one low-rank latent KV head
 // shared by every query head).
 //
-// Work unit = (shard r, request b, query i, KV split s), run by a cluster of
+// Work unit = (shard r, request b, query i, KV split s), longest request first
+// for batches up to 128, run by a cluster of
 // two CTAs.  With 128 query heads the fp32 output (128 x 512) fills a whole
 // SM's tensor memory and the bf16 query (128 x 576) does not fit next to a KV
 // ring in shared memory, so the pair splits the head dimensions:
@@ -79,6 +80,7 @@ constexpr int kLaunchRegs = 128, kCtrlRegs = 80, kSendRegs = 80, kSoftRegs = 160
 constexpr int kSplitRegs = 128 * kCtrlRegs + 256 * kSoftRegs + 128 * kSendRegs;   // 61,440
 static_assert(kSplitRegs <= 512 * kLaunchRegs, "register split exceeds the launch");
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
+constexpr int kLptMaxBatch = 128;
 // TMEM columns
 constexpr uint32_t kColQ = 0;      // 144 cols: 128 rows x 288 bf16
 constexpr uint32_t kColP = 144;    // 32 cols: 128 rows x 64 bf16
@@ -107,6 +109,7 @@ struct Smem {
   uint64_t fin;            // both softmax warpgroups posted their row sums (count 256)
   uint32_t tmem_base;
   int abort;
+  int req;                    // request of this unit
   float rmax[2][2][kHeads];   // [tile parity][warpgroup][head] partial row max
   float rsum[2][kHeads];      // [warpgroup][head] row sums, combined at the end
 };
@@ -141,6 +144,7 @@ __device__ __forceinline__ float bfp_unpack(uint32_t w, uint32_t sel, float dec,
   return fmaf(__uint_as_float(__byte_perm(w, 0x4B000000u, sel)), dec, bias);
 }
 
+template <bool kLpt>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
                 const MlaParams p) {
@@ -153,11 +157,36 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t cta = cluster_ctarank();          // 0 or 1
   const uint32_t peer = cta ^ 1u;
+  // kLpt (batches up to kLptMaxBatch): units in longest-request-first order.
+  // The block scheduler starts clusters in index order, so short units fill
+  // the tail.  Rank k of the order (length descending, index ascending) is
+  // found by counting; both CTAs of the pair compute the same request.  (The
+  // loaded request index costs registers, so large batches keep the plain
+  // order, whose indices are recomputed from the block index.)
   const long long unit = blockIdx.x >> 1;
-  const int s_idx = (int)(unit % p.n_split);
-  const int i_q = (int)((unit / p.n_split) % p.Lq);
-  const int b = (int)((unit / ((long long)p.n_split * p.Lq)) % p.B);
-  const int r = (int)(unit / ((long long)p.n_split * p.Lq * p.B));
+  int b_lpt = 0;
+  if (kLpt) {
+    const long long per_req = (long long)p.N * p.Lq * p.n_split;
+    const int k_req = (int)(unit / per_req);
+    for (int j = tid; j < p.B; j += kThreads) {
+      const int sj = p.seq_lens[j];
+      int rank = 0;
+#pragma unroll 1
+      for (int i = 0; i < p.B; ++i) {
+        const int si = p.seq_lens[i];
+        rank += (si > sj) || (si == sj && i < j);
+      }
+      if (rank == k_req) sm.req = j;
+    }
+    __syncthreads();
+    b_lpt = *(volatile int*)&sm.req;
+  }
+  const long long per_req = (long long)p.N * p.Lq * p.n_split;
+  const long long rest = kLpt ? unit % per_req : unit;
+  const int s_idx = (int)(rest % p.n_split);
+  const int i_q = (int)((rest / p.n_split) % p.Lq);
+  const int b = kLpt ? b_lpt : (int)((unit / ((long long)p.n_split * p.Lq)) % p.B);
+  const int r = kLpt ? (int)(rest / ((long long)p.n_split * p.Lq)) : (int)(unit / ((long long)p.n_split * p.Lq * p.B));
 
   // key range of this unit (shard-local indices [kb, ke))
   const int S = p.seq_lens[b];
@@ -635,17 +664,20 @@ cudaError_t launch_attn_mla_tc(const AttnArgs& a, const SplitPlan& plan) {
     p.dst_lse = a.lse;
   }
   const size_t smem = mla_smem_bytes();
+  const bool lpt = a.B <= kLptMaxBatch;
+  void (*kern)(const CUtensorMap, const CUtensorMap, const MlaParams) =
+      lpt ? mla_attn_kernel<true> : mla_attn_kernel<false>;
   // the register split assumes the compiled launch count; refuse to launch
   // otherwise (setmaxnreg.inc would wait for registers that do not exist)
   cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, mla_attn_kernel);
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
   if (fa.numRegs * (int)kThreads < kSplitRegs) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(mla_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long long units = (long long)a.N * a.B * a.Lq * plan.n_split;
   if (units == 0) return cudaSuccess;
-  mla_attn_kernel<<<(unsigned)(2 * units), kThreads, smem, a.stream>>>(tm_lat, tm_rope, p);
+  kern<<<(unsigned)(2 * units), kThreads, smem, a.stream>>>(tm_lat, tm_rope, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || plan.n_split <= 1) return e;
   return launch_split_combine(a, plan);
