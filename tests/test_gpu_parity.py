@@ -88,14 +88,14 @@ ATTN_CASES = [
     ("mla_mtp", dict(lengths=("fixed", 300), dcp_size=1)),
     ("mla_mtp", dict(lengths=("fixed", 40000))),                            # KV splits + combine
     ("mla_32", dict(batch=3, lengths=("uniform", 1, 700), dcp_size=4, interleave=3)),
-    # GQA tensor-core kernel: 2 and 4 lane groups of real rows (Lq 4 and 8 x 16 heads)
+    # GQA tensor-core kernel: one and two 64-row query tiles (Lq 4 and 8 x 16 heads)
     ("qwen_gqa", dict(batch=2, q_len=4, lengths=("uniform", 200, 1500), dcp_size=2)),
     ("qwen_gqa", dict(batch=1, q_len=8, lengths=("fixed", 3000), dcp_size=2, interleave=64)),
-    # head dims without a tensor-core kernel run on the generic SIMT kernel
-    # long causal queries (chunked prefill): several 128-row tiles per KV head
+    # long causal queries (chunked prefill): several 64-row tiles per KV head
     ("qwen_gqa", dict(batch=2, q_len=16, lengths=("uniform", 300, 1500), dcp_size=2)),
     ("qwen_gqa", dict(batch=1, q_len=40, lengths=("fixed", 2100), dcp_size=4, interleave=64)),
     ("tiny_gqa", dict(batch=2, q_len=64, lengths=("uniform", 64, 900), dcp_size=2, interleave=16)),
+    # head dims without a tensor-core kernel run on the generic SIMT kernel
     ("tiny_gqa", dict(head_dim_qk=96, head_dim_v=96, lengths=("fixed", 500))),
     ("mla_32", dict(batch=2, num_q_heads=16, head_dim_qk=72, head_dim_v=64,
                     lengths=("uniform", 100, 900), dcp_size=4)),
