@@ -106,9 +106,21 @@ SplitPlan plan_splits(const AttnArgs& a, int sm_count, int tile_tokens, int unit
   const long long target = 2LL * sm_count;
   long long n = 1;
   if (base_units < target && max_local > 4LL * tile_tokens) {
-    n = (target + base_units - 1) / base_units;
-    n = std::min<long long>(n, max_local / (4LL * tile_tokens));
-    n = std::max<long long>(1, std::min<long long>(n, 32));
+    // Split count by a wave model: units run in waves of sm_count CTAs and a
+    // unit costs its tiles plus about kUnitStartTiles of start-up and drain,
+    // so pick the count with the fewest waves x (tiles per split + start-up).
+    constexpr long long kUnitStartTiles = 4;
+    const long long tiles = (max_local + tile_tokens - 1) / tile_tokens;
+    const long long n_hi = std::max<long long>(1, std::min<long long>(32, max_local / (4LL * tile_tokens)));
+    long long best = -1;
+    for (long long c = 1; c <= n_hi; ++c) {
+      const long long waves = (base_units * c + sm_count - 1) / sm_count;
+      const long long cost = waves * ((tiles + c - 1) / c + kUnitStartTiles);
+      if (best < 0 || cost < best) {
+        best = cost;
+        n = c;
+      }
+    }
   }
   long long per = (max_local + n - 1) / n;
   per = (per + tile_tokens - 1) / tile_tokens * tile_tokens;
