@@ -466,9 +466,11 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     if (lane == 0 && T > 0) {
       constexpr uint32_t id_qk = idesc_bf16_ab(128, NCOL, false, false);
       // Each descriptor is built from its address at the MMA, in an unrolled
-      // K-step loop.  (A variant that added compile-time offsets inside a
-      // swizzle row to a 64-bit base descriptor gave wrong products on the
-      // device, although the descriptor values it printed were the same.)
+      // K-step loop.  Variants that added compile-time offsets to a run-time
+      // base descriptor here (inside a swizzle row, or whole 64-dim chunks)
+      // gave wrong products on the device, although the descriptor values
+      // they printed were the same; the PV issuer below does add offsets (whole
+      // 8-row atoms of MN-major operands), which the parity tests cover.
       const uint32_t ksteps = (uint32_t)p.D / 16;
       bool ok = true;
       for (int t = 0; t < T; ++t) {
@@ -509,11 +511,13 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         }
         tc_fence_after();
         const int st = t % p.stages;
+        // base descriptors of this stage and P^T buffer; the K-steps add whole
+        // 8-row swizzle atoms (2048 B of V, 8 rows of P^T) to the start address
+        const uint64_t dv = smem_desc(smem_u32(stages + st * stage_bytes), kChunkBytes, 1024, kSw128);
+        const uint64_t dp = smem_desc(smem_u32(ps + (t & 1) * C::kPBytes), C::kPBytes, 8 * C::kPitch, C::kPSwz);
 #pragma unroll
         for (uint32_t k = 0; k < kNt / 16; ++k)
-          mma_ss(tO, smem_desc(smem_u32(stages + st * stage_bytes + k * 2048), kChunkBytes, 1024, kSw128),
-                 smem_desc(smem_u32(ps + (t & 1) * C::kPBytes + k * 16 * C::kPitch), C::kPBytes, 8 * C::kPitch, C::kPSwz),
-                 id_pv, (t > 0 || k > 0) ? 1u : 0u);
+          mma_ss(tO, dv + ((k * 2048u) >> 4), dp + ((k * 16u * C::kPitch) >> 4), id_pv, (t > 0 || k > 0) ? 1u : 0u);
         mma_commit(smem_u32(&sm.p_free[t & 1]));
         mma_commit(smem_u32(&sm.kv_empty[st]));
       }
