@@ -8,6 +8,9 @@
 //                   B = P rows stored by threads under the NCOL-wide swizzle
 //                   (32/64/128 bytes, MN-major)
 //   D5            = the same product with P loaded by TMA under that swizzle
+//   D6, D7        = D3 with descriptors built once and advanced per K-step by
+//                   adding the byte offset >> 4 to the start address: D6 as a
+//                   64-bit add, D7 on the low 32-bit word only
 // Built by the test with nvcc; not part of libdcp.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -24,6 +27,14 @@ namespace {
 constexpr uint32_t kChunk = 128 * 128;   // 128 rows x 64 dims bf16
 constexpr uint64_t kLimitNs = 2000000000ull;
 
+// descriptor + offset on the low 32-bit word (start address field), the high
+// word (strides, version, swizzle) passed through untouched
+__device__ __forceinline__ uint64_t desc_add_lo(uint64_t d, uint32_t off) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"((uint32_t)d + off), "r"((uint32_t)(d >> 32)));
+  return r;
+}
+
 template <int NCOL>
 __device__ __forceinline__ uint32_t pchunk(uint32_t c, uint32_t k) {
   return NCOL == 16 ? (c ^ ((k >> 2) & 1u)) : NCOL == 32 ? (c ^ ((k >> 1) & 3u)) : (c ^ (k & 7u));
@@ -34,7 +45,7 @@ __global__ void __launch_bounds__(128, 1)
 umma_t_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const __grid_constant__ CUtensorMap tm_p, const __nv_bfloat16* __restrict__ Q,
               const __nv_bfloat16* __restrict__ P, float* __restrict__ D3, float* __restrict__ D4,
-              float* __restrict__ D5, int* __restrict__ status) {
+              float* __restrict__ D5, float* __restrict__ D6, float* __restrict__ D7, int* __restrict__ status) {
   constexpr uint32_t kPitch = NCOL * 2, kPBytes = 128 * kPitch;
   constexpr uint32_t kSwz = NCOL == 16 ? kSw32 : NCOL == 32 ? kSw64 : kSw128;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -55,7 +66,7 @@ umma_t_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     mbar_init(bar_mma, 1);
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 256);
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
   // Q rows (K-major, 128B swizzle) and P rows (MN-major, NCOL-wide swizzle)
   for (int idx = tid; idx < NCOL * 16; idx += 128) {
     const int h = idx / 16, ch = (idx % 16) / 8, c = idx % 8;
@@ -91,6 +102,17 @@ umma_t_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         const uint64_t b = smem_desc(smem_u32(qs + (k >> 2) * NCOL * 128 + (k & 3) * 32), 16, 1024, kSw128);
         mma_ss(tbase, a, b, id_qk, k > 0);
       }
+      // D6 / D7: base descriptors plus compile-time K-step offsets
+      const uint64_t ka = smem_desc(smem_u32(ks), 16, 1024, kSw128);
+      const uint64_t qb = smem_desc(smem_u32(qs), 16, 1024, kSw128);
+#pragma unroll
+      for (uint32_t k = 0; k < 8; ++k)
+        mma_ss(tbase + 3 * NCOL, ka + (((k >> 2) * kChunk + (k & 3) * 32) >> 4),
+               qb + (((k >> 2) * NCOL * 128 + (k & 3) * 32) >> 4), id_qk, k > 0);
+#pragma unroll
+      for (uint32_t k = 0; k < 8; ++k)
+        mma_ss(tbase + 4 * NCOL, desc_add_lo(ka, ((k >> 2) * kChunk + (k & 3) * 32) >> 4),
+               desc_add_lo(qb, ((k >> 2) * NCOL * 128 + (k & 3) * 32) >> 4), id_qk, k > 0);
       for (int k = 0; k < 8; ++k) {
         const uint64_t a = smem_desc(smem_u32(vs + k * 2048), kChunk, 1024, kSw128);
         const uint64_t b4 = smem_desc(smem_u32(pm + k * 16 * kPitch), kPBytes, 8 * kPitch, kSwz);
@@ -106,8 +128,8 @@ umma_t_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   tc_fence_after();
   const uint32_t lane_base = taddr(tbase, (uint32_t)(warp * 32), 0);
   if (__all_sync(0xffffffffu, done)) {
-    float* outs[3] = {D3, D4, D5};
-    for (int m = 0; m < 3; ++m) {
+    float* outs[5] = {D3, D4, D5, D6, D7};
+    for (int m = 0; m < 5; ++m) {
       for (int c = 0; c < NCOL / 16; ++c) {
         uint32_t r[16];
         tmem_ld16(lane_base + m * NCOL + c * 16, r);
@@ -120,11 +142,12 @@ umma_t_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tbase, 256);
+  if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
 template <int NCOL>
-int run(const void* K, const void* V, const void* Q, const void* P, float* D3, float* D4, float* D5, int* status) {
+int run(const void* K, const void* V, const void* Q, const void* P, float* D3, float* D4, float* D5, float* D6,
+        float* D7, int* status) {
   CUtensorMap tm_k, tm_v, tm_p;
   const uint64_t dims[2] = {128, 128};
   const uint64_t strides[1] = {128 * 2};
@@ -143,7 +166,7 @@ int run(const void* K, const void* V, const void* Q, const void* P, float* D3, f
   cudaError_t e = cudaFuncSetAttribute(umma_t_kernel<NCOL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return (int)e;
   umma_t_kernel<NCOL><<<1, 128, smem>>>(tm_k, tm_v, tm_p, static_cast<const __nv_bfloat16*>(Q),
-                                        static_cast<const __nv_bfloat16*>(P), D3, D4, D5, status);
+                                        static_cast<const __nv_bfloat16*>(P), D3, D4, D5, D6, D7, status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return (int)e;
   return (int)cudaDeviceSynchronize();
@@ -152,11 +175,11 @@ int run(const void* K, const void* V, const void* Q, const void* P, float* D3, f
 }  // namespace
 
 extern "C" int umma_probe_t(int ncol, const void* K, const void* V, const void* Q, const void* P, float* D3,
-                            float* D4, float* D5, int* status) {
+                            float* D4, float* D5, float* D6, float* D7, int* status) {
   switch (ncol) {
-    case 16: return run<16>(K, V, Q, P, D3, D4, D5, status);
-    case 32: return run<32>(K, V, Q, P, D3, D4, D5, status);
-    case 64: return run<64>(K, V, Q, P, D3, D4, D5, status);
+    case 16: return run<16>(K, V, Q, P, D3, D4, D5, D6, D7, status);
+    case 32: return run<32>(K, V, Q, P, D3, D4, D5, D6, D7, status);
+    case 64: return run<64>(K, V, Q, P, D3, D4, D5, D6, D7, status);
   }
   return -9;
 }

@@ -65,7 +65,7 @@ def probe_t(tmp_path_factory):
     subprocess.run(cmd, check=True, capture_output=True)
     lib = ctypes.CDLL(str(out))
     lib.umma_probe_t.restype = ctypes.c_int
-    lib.umma_probe_t.argtypes = [ctypes.c_int] + [ctypes.c_void_p] * 8
+    lib.umma_probe_t.argtypes = [ctypes.c_int] + [ctypes.c_void_p] * 10
     return lib
 
 
@@ -73,22 +73,26 @@ def probe_t(tmp_path_factory):
 def test_umma_transposed_forms(probe_t, ncol):
     """Keys-as-M forms: S^T = K Q^T (A = K tile, B = Q rows under the 128-byte
     swizzle) and O^T = V^T P^T (A = V tile read MN-major, B = P rows under the
-    ncol-wide swizzle, stored by threads and, separately, by TMA)."""
+    ncol-wide swizzle, stored by threads and, separately, by TMA); and S^T again
+    with descriptors built once and advanced per K-step by adding the offset to
+    the start-address field (as a 64-bit add and on the low word only)."""
     g = torch.Generator(device="cuda").manual_seed(11 + ncol)
     K = torch.randn((128, 128), generator=g, device="cuda").to(torch.bfloat16)
     V = torch.randn((128, 128), generator=g, device="cuda").to(torch.bfloat16)
     Q = torch.randn((ncol, 128), generator=g, device="cuda").to(torch.bfloat16)
     P = torch.rand((128, ncol), generator=g, device="cuda").to(torch.bfloat16)
-    D = [torch.full((128, ncol), float("nan"), device="cuda") for _ in range(3)]
+    D = [torch.full((128, ncol), float("nan"), device="cuda") for _ in range(5)]
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     rc = probe_t.umma_probe_t(ncol, K.data_ptr(), V.data_ptr(), Q.data_ptr(), P.data_ptr(),
-                              D[0].data_ptr(), D[1].data_ptr(), D[2].data_ptr(), status.data_ptr())
+                              D[0].data_ptr(), D[1].data_ptr(), D[2].data_ptr(), D[3].data_ptr(),
+                              D[4].data_ptr(), status.data_ptr())
     assert rc == 0, rc
     assert int(status.item()) == 0
     ref_s = K.double() @ Q.double().T
     ref_o = V.double().T @ P.double()
     for got, ref, what in ((D[0], ref_s, "S^T"), (D[1], ref_o, "O^T (P by threads)"),
-                           (D[2], ref_o, "O^T (P by TMA)")):
+                           (D[2], ref_o, "O^T (P by TMA)"), (D[3], ref_s, "S^T (64-bit descriptor advance)"),
+                           (D[4], ref_s, "S^T (low-word descriptor advance)")):
         assert torch.isfinite(got).all(), what
         err = (got.double() - ref).abs().max().item()
         assert err < 1e-3 * ref.abs().max().item(), (what, err)
