@@ -97,6 +97,13 @@ ATTN_CASES = [
     ("tiny_gqa", dict(batch=2, q_len=64, lengths=("uniform", 64, 900), dcp_size=2, interleave=16)),
     # head dims without a tensor-core kernel run on the generic SIMT kernel
     ("tiny_gqa", dict(head_dim_qk=96, head_dim_v=96, lengths=("fixed", 500))),
+    # GQA block sizes: several TMA boxes per 128-key tile (8, 32, 64), a block
+    # spanning two tiles (256), and one the tensor-core kernel declines (48)
+    ("qwen_gqa", dict(batch=2, block_size=8, lengths=("uniform", 300, 1300), dcp_size=2)),
+    ("qwen_gqa", dict(batch=2, block_size=32, lengths=("uniform", 300, 1300), dcp_size=4, interleave=32)),
+    ("qwen_gqa", dict(batch=2, block_size=64, lengths=("uniform", 700, 2000), dcp_size=2, interleave=64)),
+    ("qwen_gqa", dict(batch=2, block_size=256, lengths=("uniform", 700, 3000), dcp_size=2, interleave=256)),
+    ("tiny_gqa", dict(block_size=48, lengths=("fixed", 700), dcp_size=2, interleave=48)),
     ("mla_32", dict(batch=2, num_q_heads=16, head_dim_qk=72, head_dim_v=64,
                     lengths=("uniform", 100, 900), dcp_size=4)),
 ]
