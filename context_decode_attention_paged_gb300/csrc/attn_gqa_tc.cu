@@ -21,15 +21,16 @@
 // the pool [block*block_size][Hkv][D] selects KV head g, so any block size that
 // is a multiple of 8 and divides (or is a multiple of) 128 works.
 //
-// Softmax: thread k of the four softmax warps owns key k of the tile and the
-// scores of that key for every query row.  The reference max of each row is
+// Softmax: a thread owns key k of the tile and the scores of that key for half
+// of the query rows.  The reference max of each row is
 // shared by all threads and moves lazily: one barrier per tile ORs "some score
 // exceeds its row's reference by more than 2^8"; only then do the warps reduce
 // the tile's row maxima, rescale O^T (after the previous PV has landed) and
 // their per-thread row sums.  Row sums are reduced across the 128 key threads
 // once, at the end.  Logs are base 2 with the scale folded into the exponent.
-// Warp roles (224 threads): warp 0 TMA producer, warp 1 QK issuer and TMEM
-// owner, warp 2 PV issuer, warps 3..6 softmax/epilogue.  A tcgen05.mma takes
+// Warp roles (352 threads): warp 0 TMA producer, warp 1 QK issuer and TMEM
+// owner, warp 2 PV issuer, warps 3..10 softmax/epilogue (two per TMEM lane
+// quadrant, each taking half of the query-row columns).  A tcgen05.mma takes
 // one issuing thread tens of cycles, so QK and PV have a thread each (PV(t)
 // goes out as soon as P(t) is ready, not after the next tile's QK).
 // Every wait is bounded; on expiry the
@@ -51,7 +52,9 @@ using namespace sm100;
 constexpr int kNt = 128;                       // keys per tile (MMA M of S^T)
 constexpr int kMaxStages = 6;
 constexpr uint32_t kChunkBytes = kNt * 128;    // 128 keys x 64 dims bf16
-constexpr uint32_t kThreads = 224;
+constexpr int kFirstSoftWarp = 3;             // warps 3..10: softmax
+constexpr uint32_t kSoftThreads = 256;
+constexpr uint32_t kThreads = 96 + kSoftThreads;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxCols = 64;                   // query rows per row tile
@@ -118,47 +121,65 @@ size_t gqa_smem_bytes(int D, int ncol, int stages) {
   return gqa_fixed_bytes(D, ncol) + (size_t)stages * gqa_stage_bytes(D);
 }
 
-// Softmax and epilogue of the four softmax warps (thread = TMEM lane: key k of
-// the tile for S^T and P^T, value dim k for O^T).
+// Softmax and epilogue of the eight softmax warps: two per TMEM lane quadrant,
+// each taking half of the query-row columns (thread = TMEM lane: key k of the
+// tile for S^T and P^T, value dim k for O^T; columns [h0, h0 + HC)).
 template <int NCOL, typename Fail>
 __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, uint8_t* stages,
                                                  uint32_t stage_bytes, uint8_t* ps, uint32_t tmem, int warp,
                                                  int lane, int T, int kb, int ke, int lim_min, int R, int row0,
                                                  int gsize, int g, int b, int r, int s_idx, Fail fail) {
   using C = Cfg<NCOL>;
+  constexpr int HC = NCOL / 2;                            // columns per thread
   const int nch = p.D / 64;
   const int qd = warp & 3;                                // TMEM lane quadrant of this warp
+  const int h0 = ((warp - kFirstSoftWarp) >> 2) * HC;     // first column of this warp
   const int lrow = qd * 32 + lane;
   const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
-  const uint32_t tO = lane_base + 2 * NCOL;
+  const uint32_t tO = lane_base + 2 * NCOL + h0;
   volatile int* abort_flag = &sm.abort;
-  float m[NCOL], l[NCOL];
+  float m[HC], l[HC];
 #pragma unroll
-  for (int h = 0; h < NCOL; ++h) {
+  for (int h = 0; h < HC; ++h) {
     m[h] = -INFINITY;
     l[h] = 0.f;
   }
+  auto ld_cols = [&](uint32_t addr, uint32_t (&v)[HC]) {
+    if constexpr (HC == 8) {
+      tmem_ld8(addr, v);
+    } else {
+#pragma unroll
+      for (int c = 0; c < HC / 16; ++c) tmem_ld16(addr + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&v[16 * c]));
+    }
+  };
+  auto st_cols = [&](uint32_t addr, const uint32_t (&v)[HC]) {
+    if constexpr (HC == 8) {
+      tmem_st8(addr, v);
+    } else {
+#pragma unroll
+      for (int c = 0; c < HC / 16; ++c)
+        tmem_st16(addr + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(&v[16 * c]));
+    }
+  };
   bool bad = false, broke = false;
   for (int t = 0; t < T; ++t) {
     const int bsel = t & 1;
     const bool okw = __all_sync(0xffffffffu, *abort_flag == 0 &&
                                                  mbar_wait(smem_u32(&sm.s_full[bsel]), (uint32_t)(t >> 1) & 1u, kWaitNs));
     if (!okw) bad = true;
-    float x[NCOL];
+    float x[HC];
     {
-      uint32_t v[NCOL];
+      uint32_t v[HC];
       if (okw) {
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < NCOL / 16; ++c)
-          tmem_ld16(lane_base + bsel * NCOL + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&v[16 * c]));
+        ld_cols(lane_base + bsel * NCOL + h0, v);
         tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int h = 0; h < NCOL; ++h) v[h] = 0u;
+        for (int h = 0; h < HC; ++h) v[h] = 0u;
       }
 #pragma unroll
-      for (int h = 0; h < NCOL; ++h) x[h] = __uint_as_float(v[h]);
+      for (int h = 0; h < HC; ++h) x[h] = __uint_as_float(v[h]);
     }
     tc_fence_before();
     mbar_arrive(smem_u32(&sm.s_free[bsel]));
@@ -170,30 +191,30 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
     float e = -INFINITY;
     if (full) {
 #pragma unroll
-      for (int h = 0; h < NCOL; ++h) {
+      for (int h = 0; h < HC; ++h) {
         x[h] *= p.scale_log2;
         e = fmaxf(e, x[h] - m[h]);
       }
     } else {
 #pragma unroll
-      for (int h = 0; h < NCOL; ++h) {
-        x[h] = jj < sm.lim[h] ? x[h] * p.scale_log2 : -INFINITY;
+      for (int h = 0; h < HC; ++h) {
+        x[h] = jj < sm.lim[h0 + h] ? x[h] * p.scale_log2 : -INFINITY;
         e = fmaxf(e, x[h] - m[h]);
       }
     }
     // one barrier per tile: does any row's reference max have to move?
-    if (bar_red_or(kBarSoftmax, 128, e > kRescaleLog2 || bad)) {
-      if (bar_red_or(kBarSoftmax, 128, bad)) {
+    if (bar_red_or(kBarSoftmax, kSoftThreads, e > kRescaleLog2 || bad)) {
+      if (bar_red_or(kBarSoftmax, kSoftThreads, bad)) {
         broke = true;
         break;
       }
-      // row maxima of the tile over its 128 keys
+      // row maxima of the tile over its 128 keys (the four quadrant warps of a column)
 #pragma unroll
-      for (int h = 0; h < NCOL; ++h) {
+      for (int h = 0; h < HC; ++h) {
         float v = x[h];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-        if (lane == 0) sm.red[qd][h] = v;
+        if (lane == 0) sm.red[qd][h0 + h] = v;
       }
       // O^T is rescaled below: the previous tile's PV must have landed.  Its
       // P^T buffer's barrier is at most one phase ahead of what this thread
@@ -201,14 +222,15 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
       if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_free[(t - 1) & 1]),
                                                       (uint32_t)((t - 1) >> 1) & 1u, kWaitNs)))
         bad = true;
-      if (bar_red_or(kBarSoftmax, 128, bad)) {
+      if (bar_red_or(kBarSoftmax, kSoftThreads, bad)) {
         broke = true;
         break;
       }
-      float alpha[NCOL];
+      float alpha[HC];
 #pragma unroll
-      for (int h = 0; h < NCOL; ++h) {
-        const float tmax = fmaxf(fmaxf(sm.red[0][h], sm.red[1][h]), fmaxf(sm.red[2][h], sm.red[3][h]));
+      for (int h = 0; h < HC; ++h) {
+        const int hh = h0 + h;
+        const float tmax = fmaxf(fmaxf(sm.red[0][hh], sm.red[1][hh]), fmaxf(sm.red[2][hh], sm.red[3][hh]));
         const float mn = fmaxf(m[h], tmax);
         alpha[h] = m[h] == -INFINITY ? 0.f : ex2(m[h] - mn);
         m[h] = mn;
@@ -216,24 +238,21 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
       }
       if (t > 0) {
         tc_fence_after();
+        uint32_t o[HC];
+        ld_cols(tO, o);
+        tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < NCOL / 16; ++c) {
-          uint32_t o[16];
-          tmem_ld16(tO + 16 * c, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha[16 * c + k]);
-          tmem_st16(tO + 16 * c, o);
-        }
+        for (int k = 0; k < HC; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha[k]);
+        st_cols(tO, o);
         tmem_wait_st();
       }
     }
 
-    // this key's probabilities for every row -> its P^T row (bf16)
-    uint32_t pk[NCOL / 2];
+    // this key's probabilities for this warp's rows -> its half of the P^T row (bf16)
+    uint32_t pk[HC / 2];
     if (full) {
 #pragma unroll
-      for (int h = 0; h < NCOL; h += 2) {
+      for (int h = 0; h < HC; h += 2) {
         const float p0 = ex2(x[h] - m[h]), p1 = ex2(x[h + 1] - m[h + 1]);
         l[h] += p0;
         l[h + 1] += p1;
@@ -241,7 +260,7 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
       }
     } else {
 #pragma unroll
-      for (int h = 0; h < NCOL; h += 2) {
+      for (int h = 0; h < HC; h += 2) {
         const float p0 = x[h] == -INFINITY ? 0.f : ex2(x[h] - m[h]);
         const float p1 = x[h + 1] == -INFINITY ? 0.f : ex2(x[h + 1] - m[h + 1]);
         l[h] += p0;
@@ -254,10 +273,10 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
       bad = true;
     uint8_t* prow = ps + bsel * C::kPBytes + lrow * C::kPitch;
 #pragma unroll
-    for (int c = 0; c < NCOL / 8; ++c)
-      *reinterpret_cast<uint4*>(prow + (C::pchunk((uint32_t)c, (uint32_t)lrow) << 4)) =
+    for (int c = 0; c < HC / 8; ++c)
+      *reinterpret_cast<uint4*>(prow + (C::pchunk((uint32_t)(h0 / 8 + c), (uint32_t)lrow) << 4)) =
           make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-    if (jj >= ke) {
+    if (h0 == 0 && jj >= ke) {
       // key past the range (ragged last tile): zero its value row so that
       // 0 * (NaN/Inf) from a stale cache slot cannot reach O
       uint8_t* vt = stages + (t % p.stages) * stage_bytes + lrow * 128;
@@ -277,35 +296,35 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
   if (have && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_free[(T - 1) & 1]),
                                                  (uint32_t)((T - 1) >> 1) & 1u, kWaitNs)))
     bad = true;
-  if (bar_red_or(kBarSoftmax, 128, bad)) have = false;
+  if (bar_red_or(kBarSoftmax, kSoftThreads, bad)) have = false;
   if (bad) fail();
 
-  // row sums over the 128 key threads
+  // row sums over the 128 key threads (the four quadrant warps of a column)
 #pragma unroll
-  for (int h = 0; h < NCOL; ++h) {
+  for (int h = 0; h < HC; ++h) {
     float v = l[h];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    if (lane == 0) sm.red[qd][h] = v;
+    if (lane == 0) sm.red[qd][h0 + h] = v;
   }
-  named_bar_sync(kBarSoftmax, 128);
+  named_bar_sync(kBarSoftmax, kSoftThreads);
 
-  // outputs: this thread holds value dim lrow of every row
-  uint32_t o[NCOL];
+  // outputs: this thread holds value dim lrow of this warp's rows
+  uint32_t o[HC];
 #pragma unroll
-  for (int h = 0; h < NCOL; ++h) o[h] = 0u;
+  for (int h = 0; h < HC; ++h) o[h] = 0u;
   if (have) {
     tc_fence_after();
-#pragma unroll
-    for (int c = 0; c < NCOL / 16; ++c) tmem_ld16(tO + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&o[16 * c]));
+    ld_cols(tO, o);
     tmem_wait_ld();
   }
 #pragma unroll
-  for (int h = 0; h < NCOL; ++h) {
-    if (h < R) {
-      const float lsum = (sm.red[0][h] + sm.red[1][h]) + (sm.red[2][h] + sm.red[3][h]);
+  for (int h = 0; h < HC; ++h) {
+    const int hh = h0 + h;
+    if (hh < R) {
+      const float lsum = (sm.red[0][hh] + sm.red[1][hh]) + (sm.red[2][hh] + sm.red[3][hh]);
       const bool live = have && lsum > 0.f;
-      const int rr = row0 + h, i = rr / gsize, head = g * gsize + rr % gsize;
+      const int rr = row0 + hh, i = rr / gsize, head = g * gsize + rr % gsize;
       const long long urow = ((((long long)r * p.B + b) * p.Lq + i) * p.n_split + s_idx) * p.Hq + head;
       if (lrow < p.D) p.dst_o[urow * p.D + lrow] = live ? __uint_as_float(o[h]) * (1.f / lsum) : 0.f;
       if (lrow == 0) p.dst_lse[urow] = live ? (m[h] + log2f(lsum)) * 0.69314718055994531f : -INFINITY;
@@ -379,8 +398,8 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(smem_u32(&sm.s_full[k]), 1);
-      mbar_init(smem_u32(&sm.s_free[k]), 128);
-      mbar_init(smem_u32(&sm.p_full[k]), 128);
+      mbar_init(smem_u32(&sm.s_free[k]), kSoftThreads);
+      mbar_init(smem_u32(&sm.p_full[k]), kSoftThreads);
       mbar_init(smem_u32(&sm.p_free[k]), 1);
     }
     mbar_init(smem_u32(&sm.drain[0]), 1);
@@ -389,12 +408,12 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(&sm.tmem_base), C::kTmemCols);
-  if (warp >= 3) {
+  if (warp >= kFirstSoftWarp) {
     // Q^T rows -> smem, K-major with the 128-byte swizzle (rows >= R are zero),
     // and the causal key limit of every row
-    const int st = tid - 96;
+    const int st = tid - 32 * kFirstSoftWarp;
     const int per_row = nch * 8;                          // 16-byte chunks of a row
-    for (int idx = st; idx < NCOL * per_row; idx += 128) {
+    for (int idx = st; idx < NCOL * per_row; idx += (int)kSoftThreads) {
       const int h = idx / per_row, ch = (idx % per_row) >> 3, c = idx & 7;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (h < R && !bad_len) {
