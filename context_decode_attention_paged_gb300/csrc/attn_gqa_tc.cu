@@ -21,16 +21,16 @@
 // the pool [block*block_size][Hkv][D] selects KV head g, so any block size that
 // is a multiple of 8 and divides (or is a multiple of) 128 works.
 //
-// Softmax: a thread owns key k of the tile and the scores of that key for half
-// of the query rows.  The reference max of each row is
+// Softmax: a thread owns key k of the tile and the scores of that key for a
+// quarter of the query rows.  The reference max of each row is
 // shared by all threads and moves lazily: one barrier per tile ORs "some score
 // exceeds its row's reference by more than 2^8"; only then do the warps reduce
 // the tile's row maxima, rescale O^T (after the previous PV has landed) and
 // their per-thread row sums.  Row sums are reduced across the 128 key threads
 // once, at the end.  Logs are base 2 with the scale folded into the exponent.
-// Warp roles (352 threads): warp 0 TMA producer, warp 1 QK issuer and TMEM
-// owner, warp 2 PV issuer, warps 3..10 softmax/epilogue (two per TMEM lane
-// quadrant, each taking half of the query-row columns).  A tcgen05.mma takes
+// Warp roles (608 threads): warp 0 TMA producer, warp 1 QK issuer and TMEM
+// owner, warp 2 PV issuer, warps 3..18 softmax/epilogue (four per TMEM lane
+// quadrant, each taking a quarter of the query-row columns).  A tcgen05.mma takes
 // one issuing thread tens of cycles, so QK and PV have a thread each (PV(t)
 // goes out as soon as P(t) is ready, not after the next tile's QK).
 // Every wait is bounded; on expiry the
@@ -52,8 +52,9 @@ using namespace sm100;
 constexpr int kNt = 128;                       // keys per tile (MMA M of S^T)
 constexpr int kMaxStages = 6;
 constexpr uint32_t kChunkBytes = kNt * 128;    // 128 keys x 64 dims bf16
-constexpr int kFirstSoftWarp = 3;             // warps 3..10: softmax
-constexpr uint32_t kSoftThreads = 256;
+constexpr int kFirstSoftWarp = 3;             // warps 3.. : softmax
+constexpr int kSoftGroups = 4;                 // softmax warps per TMEM lane quadrant
+constexpr uint32_t kSoftThreads = 128 * kSoftGroups;
 constexpr uint32_t kThreads = 96 + kSoftThreads;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescaleLog2 = 8.0f;
@@ -121,16 +122,17 @@ size_t gqa_smem_bytes(int D, int ncol, int stages) {
   return gqa_fixed_bytes(D, ncol) + (size_t)stages * gqa_stage_bytes(D);
 }
 
-// Softmax and epilogue of the eight softmax warps: two per TMEM lane quadrant,
-// each taking half of the query-row columns (thread = TMEM lane: key k of the
-// tile for S^T and P^T, value dim k for O^T; columns [h0, h0 + HC)).
+// Softmax and epilogue of the softmax warps: kSoftGroups per TMEM lane
+// quadrant, each taking an equal share of the query-row columns (thread = TMEM
+// lane: key k of the tile for S^T and P^T, value dim k for O^T; columns
+// [h0, h0 + HC)).
 template <int NCOL, typename Fail>
 __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, uint8_t* stages,
                                                  uint32_t stage_bytes, uint8_t* ps, uint32_t tmem, int warp,
                                                  int lane, int T, int kb, int ke, int lim_min, int R, int row0,
                                                  int gsize, int g, int b, int r, int s_idx, Fail fail) {
   using C = Cfg<NCOL>;
-  constexpr int HC = NCOL / 2;                            // columns per thread
+  constexpr int HC = NCOL / kSoftGroups;                  // columns per thread
   const int nch = p.D / 64;
   const int qd = warp & 3;                                // TMEM lane quadrant of this warp
   const int h0 = ((warp - kFirstSoftWarp) >> 2) * HC;     // first column of this warp
@@ -145,7 +147,9 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
     l[h] = 0.f;
   }
   auto ld_cols = [&](uint32_t addr, uint32_t (&v)[HC]) {
-    if constexpr (HC == 8) {
+    if constexpr (HC == 4) {
+      tmem_ld4(addr, v);
+    } else if constexpr (HC == 8) {
       tmem_ld8(addr, v);
     } else {
 #pragma unroll
@@ -153,7 +157,9 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
     }
   };
   auto st_cols = [&](uint32_t addr, const uint32_t (&v)[HC]) {
-    if constexpr (HC == 8) {
+    if constexpr (HC == 4) {
+      tmem_st4(addr, v);
+    } else if constexpr (HC == 8) {
       tmem_st8(addr, v);
     } else {
 #pragma unroll
@@ -272,10 +278,16 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
         !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_free[bsel]), (uint32_t)((t >> 1) - 1) & 1u, kWaitNs)))
       bad = true;
     uint8_t* prow = ps + bsel * C::kPBytes + lrow * C::kPitch;
+    if constexpr (HC == 4) {
+      // half of a 16-byte chunk: the swizzle moves whole chunks
+      *reinterpret_cast<uint2*>(prow + (C::pchunk((uint32_t)(h0 / 8), (uint32_t)lrow) << 4) + (h0 % 8) * 2) =
+          make_uint2(pk[0], pk[1]);
+    } else {
 #pragma unroll
-    for (int c = 0; c < HC / 8; ++c)
-      *reinterpret_cast<uint4*>(prow + (C::pchunk((uint32_t)(h0 / 8 + c), (uint32_t)lrow) << 4)) =
-          make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      for (int c = 0; c < HC / 8; ++c)
+        *reinterpret_cast<uint4*>(prow + (C::pchunk((uint32_t)(h0 / 8 + c), (uint32_t)lrow) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    }
     if (h0 == 0 && jj >= ke) {
       // key past the range (ragged last tile): zero its value row so that
       // 0 * (NaN/Inf) from a stale cache slot cannot reach O
