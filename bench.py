@@ -77,7 +77,7 @@ def algorithmic(w: wl.Workload, seq_lens) -> dict:
 # were taken on: once the source changes, traffic is reported as null.
 NCU_TRAFFIC_RATIO = {
     "mla": ("c9bdc47fcde8925c", 1.00747, "attn_mla_tc.cu"),   # mla_attn_kernel_mla32_full.md
-    "gqa": ("679c41c9f8c9111e", 1.00388, "attn_gqa_tc.cu"),   # gqa_attn_kernel_qwen_full.md
+    "gqa": ("de022da015e73ab4", 1.00383, "attn_gqa_tc.cu"),   # gqa_attn_kernel_qwen_full.md
 }
 
 
