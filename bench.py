@@ -486,6 +486,7 @@ def run_ours(args):
     roof.update({"traffic": measured_traffic(w.kind, alg["attn_bytes"]), "peak_source": f"{peak_src} (MEASURED_PEAKS.json)"
                  if peak_src == "measured" else "fallback",
                  "kernel": "dcp_decode_attn", "attn_ms": round(attn_avg, 4),
+                 "attn_ms_median": round(statistics.median(attn_ms), 4),
                  "merge_ms": round(statistics.mean(merge_ms), 4),
                  "alg_bytes_per_launch": alg["attn_bytes"], "alg_flops_per_launch": alg["flops"],
                  "step_frac_of_roofline": round(t_roof_ms / (ms_per_step), 4)})
@@ -516,7 +517,8 @@ def run_ours(args):
         secs, kvb, nseq, qtok = oracle_time(inst, args.cpu_budget, args.cpu_max_seqs)
         result["cpu_baseline"] = {
             "value": round(kvb / secs / 1e9, 4), "unit": "GB/s", "cores": cpu_threads(),
-            "kind": "oracle",
+            "kind": "oracle", "cpu_count": os.cpu_count(),
+            "omp_num_threads": os.environ.get("OMP_NUM_THREADS"),
             "sample": f"{nseq} request(s) of {w.name} ({kvb / 1e9:.2f} GB of cache, all "
                       f"{w.dcp_size} shards + merge), numpy fp64, {secs:.1f} s",
             "query_tokens_per_s": round(qtok / secs, 4)}
@@ -556,7 +558,8 @@ def run_reference(args):
         "config": {"workload": w.name, "kind": w.kind, "batch": w.batch, "q_len": w.q_len,
                    "dcp_size": w.dcp_size, "interleave": w.interleave},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cpu_threads(),
-                         "kind": "oracle",
+                         "kind": "oracle", "cpu_count": os.cpu_count(),
+                         "omp_num_threads": os.environ.get("OMP_NUM_THREADS"),
                          "sample": f"{nseq} request(s) of {w.name} over {args.steps} steps "
                                    f"({kvb / 1e9:.2f} GB of cache)"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
