@@ -104,6 +104,10 @@ ATTN_CASES = [
     ("qwen_gqa", dict(batch=2, block_size=64, lengths=("uniform", 700, 2000), dcp_size=2, interleave=64)),
     ("qwen_gqa", dict(batch=2, block_size=256, lengths=("uniform", 700, 3000), dcp_size=2, interleave=256)),
     ("tiny_gqa", dict(block_size=48, lengths=("fixed", 700), dcp_size=2, interleave=48)),
+    # group sizes: 1 (one real row of a 16-row tile) and 8 with Lq 3 (24 rows of a 32-row tile)
+    ("qwen_gqa", dict(batch=2, num_q_heads=8, num_kv_heads=8, lengths=("uniform", 300, 900), dcp_size=2)),
+    ("qwen_gqa", dict(batch=2, num_q_heads=32, num_kv_heads=4, q_len=3, lengths=("uniform", 300, 900),
+                      dcp_size=4)),
     ("mla_32", dict(batch=2, num_q_heads=16, head_dim_qk=72, head_dim_v=64,
                     lengths=("uniform", 100, 900), dcp_size=4)),
 ]
