@@ -68,7 +68,8 @@ bool mla_tc_supported(const AttnArgs& a);
 SplitPlan plan_attn_mla_tc(const AttnArgs& a, int sm_count);
 cudaError_t launch_attn_mla_tc(const AttnArgs& a, const SplitPlan& p);
 
-// GQA on tcgen05 (head dim 64/128, Lq * Hq/Hkv <= 128, block size multiple of 8).
+// GQA on tcgen05 (head dim 64/128, any Lq * Hq/Hkv in row tiles of up to 64, block size a
+// multiple of 8 that divides or is a multiple of 128).
 bool gqa_tc_supported(const AttnArgs& a);
 SplitPlan plan_attn_gqa_tc(const AttnArgs& a, int sm_count);
 cudaError_t launch_attn_gqa_tc(const AttnArgs& a, const SplitPlan& p);
