@@ -8,6 +8,7 @@ import os
 import re
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "dcp.h")
@@ -147,3 +148,45 @@ def _kvw(lib, desc, new_k=FAKE, new_v=FAKE, cache=FAKE, dcp_size=2, interleave=1
 ])
 def test_kv_cache_write_rejects_bad_arguments(lib, kw, extra):
     assert _kvw(lib, _desc(lib, **kw), **extra) == lib.DCP_ERR_INVALID_ARG
+
+
+def _sm_count():
+    if torch.cuda.is_available():
+        return torch.cuda.get_device_properties(0).multi_processor_count
+    return 148          # the library's answer when no device is visible
+
+
+def _wave_model_splits(base_units, max_local, tile, sm):
+    """The split count the planner documents: fewest waves x (tiles per split
+    + 4 tiles of start-up) over 1..32 splits, when the units fill less than two
+    waves; then rounded to whole tiles per split."""
+    n = 1
+    if base_units < 2 * sm and max_local > 4 * tile:
+        tiles = -(-max_local // tile)
+        best = None
+        for c in range(1, max(1, min(32, max_local // (4 * tile))) + 1):
+            cost = -(-base_units * c // sm) * (-(-tiles // c) + 4)
+            if best is None or cost < best:
+                best, n = cost, c
+    per = -(-max_local // n)
+    per = max(tile, -(-per // tile) * tile)
+    return -(-max_local // per)
+
+
+@pytest.mark.parametrize("kw,N,tile,units_per_split", [
+    # MLA long MTP request: 8 shards x 4 queries, clusters of two CTAs, 64-token tiles
+    (dict(kind="mla", batch=1, q_len=4, num_q_heads=128, num_kv_heads=1, head_dim_qk=576, head_dim_v=512,
+          block_size=128, num_blocks=8 * 196, max_local_blocks=196), 8, 64, 8),
+    # Qwen-like GQA, two short requests: 4 shards x 4 KV heads, 128-key tiles
+    (dict(kind="gqa", batch=2, q_len=1, num_q_heads=64, num_kv_heads=4, head_dim_qk=128, head_dim_v=128,
+          block_size=128, num_blocks=4 * 2 * 20, max_local_blocks=20), 4, 128, 4),
+])
+def test_split_planner_follows_the_wave_model(lib, kw, N, tile, units_per_split):
+    desc = _desc(lib, **kw)
+    ws = lib.raw_lib().dcp_decode_attn_workspace_size(ctypes.byref(desc), N)
+    n = _wave_model_splits(N * kw["batch"] * units_per_split, kw["max_local_blocks"] * kw["block_size"], tile,
+                           _sm_count())
+    rows = N * kw["batch"] * kw["q_len"] * kw["num_q_heads"]
+    want = 0 if n == 1 else ((rows * n * kw["head_dim_v"] * 4 + 255) & ~255) + rows * n * 4
+    assert n > 1
+    assert ws == want, (ws, want, n)
