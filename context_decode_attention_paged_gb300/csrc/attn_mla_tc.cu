@@ -135,13 +135,43 @@ __device__ __forceinline__ void bfp_scales(float amax, float& enc, float& dec) {
   dec = __uint_as_float((uint32_t)(eb - 13) << 23);
 }
 
-__device__ __forceinline__ uint32_t bfp_pack2(float a, float b, float enc) {
-  return __byte_perm(__float_as_uint(fmaf(a, enc, kEncMagic)), __float_as_uint(fmaf(b, enc, kEncMagic)), 0x5410);
+// Paired fp32 arithmetic (one instruction for two lanes of a register pair;
+// each half rounds exactly like the scalar fmaf / add).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
 }
 
-// low (sel 0x7610) or high (sel 0x7632) 16-bit code of w, decoded
-__device__ __forceinline__ float bfp_unpack(uint32_t w, uint32_t sel, float dec, float bias) {
-  return fmaf(__uint_as_float(__byte_perm(w, 0x4B000000u, sel)), dec, bias);
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// three-input maximum
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bfp_pack2(float a, float b, float enc) {
+  const float2 e = ffma2(make_float2(a, b), make_float2(enc, enc), make_float2(kEncMagic, kEncMagic));
+  return __byte_perm(__float_as_uint(e.x), __float_as_uint(e.y), 0x5410);
+}
+
+// both 16-bit codes of w, decoded (exact)
+__device__ __forceinline__ float2 bfp_unpack2(uint32_t w, float dec, float bias) {
+  return ffma2(make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7610)),
+                           __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7632))),
+               make_float2(dec, dec), make_float2(bias, bias));
 }
 
 template <bool kLpt>
@@ -413,8 +443,9 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
           const uint32_t wq[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            x[8 * k + 2 * j] += bfp_unpack(wq[j], 0x7610u, dec, bias);
-            x[8 * k + 2 * j + 1] += bfp_unpack(wq[j], 0x7632u, dec, bias);
+            const float2 s = fadd2(make_float2(x[8 * k + 2 * j], x[8 * k + 2 * j + 1]), bfp_unpack2(wq[j], dec, bias));
+            x[8 * k + 2 * j] = s.x;
+            x[8 * k + 2 * j + 1] = s.y;
           }
         }
       }
@@ -425,7 +456,9 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (full) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) m4[k & 3] = fmaxf(m4[k & 3], x[k]);
+        for (int k = 0; k < 32; k += 8)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) m4[j] = fmax3(m4[j], x[k + j], x[k + 4 + j]);
       } else {
 #pragma unroll
         for (int k = 0; k < 32; ++k) m4[k & 3] = fmaxf(m4[k & 3], (k < valid) ? x[k] : -INFINITY);
@@ -449,13 +482,17 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       uint32_t pk[16];
       float l4[4] = {0.f, 0.f, 0.f, 0.f};
       if (full) {
+        float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
-          const float p0 = ex2(fmaf(x[k], sl2, nm));
-          const float p1 = ex2(fmaf(x[k + 1], sl2, nm));
-          l4[(k >> 1) & 3] += p0 + p1;
+          const float2 y = ffma2(make_float2(x[k], x[k + 1]), make_float2(sl2, sl2), make_float2(nm, nm));
+          const float p0 = ex2(y.x);
+          const float p1 = ex2(y.y);
+          if ((k >> 1) & 1) lb = fadd2(lb, make_float2(p0, p1));
+          else la = fadd2(la, make_float2(p0, p1));
           pk[k / 2] = pack_bf16x2(p0, p1);
         }
+        l4[0] = la.x; l4[1] = la.y; l4[2] = lb.x; l4[3] = lb.y;
       } else {
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
@@ -580,7 +617,7 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
       for (int k = 0; k < 8; ++k) a8[k] = fmaxf(fabsf(__uint_as_float(v0[k])), fabsf(__uint_as_float(v1[k])));
 #pragma unroll
       for (int k = 8; k < 32; ++k)
-        a8[k & 7] = fmaxf(a8[k & 7], fmaxf(fabsf(__uint_as_float(v0[k])), fabsf(__uint_as_float(v1[k]))));
+        a8[k & 7] = fmax3(a8[k & 7], fabsf(__uint_as_float(v0[k])), fabsf(__uint_as_float(v1[k])));
       const float amax = fmaxf(fmaxf(fmaxf(a8[0], a8[1]), fmaxf(a8[2], a8[3])),
                                fmaxf(fmaxf(a8[4], a8[5]), fmaxf(a8[6], a8[7])));
       float enc, dec;
