@@ -73,6 +73,13 @@ WORKLOADS = {
         head_dim_qk=576, head_dim_v=512, block_size=128, dcp_size=8, interleave=128,
         scale=1.0 / math.sqrt(192.0), std=0.5,
         lengths=("lognormal", 67000, 0.25, 4096, 200000), permute_blocks=True, seed=1004),
+    # length stress variant of mla_512: log-normal sigma 1.0 (same median and
+    # clip), ~51 GB of cache; reported beside the main workload
+    "mla_512_s1": Workload(
+        "mla_512_s1", "mla", batch=512, q_len=1, num_q_heads=128, num_kv_heads=1,
+        head_dim_qk=576, head_dim_v=512, block_size=128, dcp_size=8, interleave=128,
+        scale=1.0 / math.sqrt(192.0), std=0.5,
+        lengths=("lognormal", 67000, 1.0, 4096, 200000), permute_blocks=True, seed=1005),
 }
 
 
