@@ -3,7 +3,8 @@ configuration bench.py times.
 
 The whole decode step (all shards, one attention launch, one merge launch) runs
 on the device over the full synthetic workload, generated exactly as the
-benchmark generates it.  Every request (a seeded 64 of the 512 at batch 512) is
+benchmark generates it.  Every request (at batch 512 a seeded 64 of the 512,
+always including the longest and the shortest) is
 then checked element by element against the oracle, run a few requests at a
 time on a compact host copy of their cache blocks; properties that hold at any size are checked on
 every output: everything finite, every partial LSE finite (every shard of these
@@ -24,7 +25,7 @@ from oracle import dcp_oracle as orc
 
 pytestmark = pytest.mark.gpu
 
-FULL = ["qwen_gqa", "mla_32", "mla_mtp", "mla_512"]
+FULL = ["qwen_gqa", "mla_32", "mla_mtp", "mla_512", "mla_512_s1"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -36,11 +37,18 @@ def _lib():
 
 
 def _checked_requests(w: wl.Workload):
-    """Every request, except at batch 512: a seeded subset of 64."""
+    """Every request, except at batch 512: a seeded subset of 64 that always
+    holds the longest and the shortest request."""
     if w.batch <= 64:
         return list(range(w.batch))
     rng = np.random.default_rng(20260 + w.batch)
-    return sorted(rng.choice(w.batch, size=64, replace=False).tolist())
+    idx = set(rng.choice(w.batch, size=62, replace=False).tolist())
+    lens = wl.make_seq_lens(w)
+    idx.add(int(torch.argmax(lens)))
+    idx.add(int(torch.argmin(lens)))
+    while len(idx) < 64:
+        idx.add(int(rng.integers(w.batch)))
+    return sorted(idx)
 
 
 @pytest.mark.parametrize("name", FULL)
