@@ -79,7 +79,7 @@ def algorithmic(w: wl.Workload, seq_lens) -> dict:
 # with the cache bytes processed).  Keyed by the kernel source the counters
 # were taken on: once the source changes, traffic is reported as null.
 NCU_TRAFFIC_RATIO = {
-    "mla": ("22fd0d3ef767e55c", 1.00737, "attn_mla_tc.cu"),   # mla_attn_kernel_mla32_full.md
+    "mla": ("72df035987125067", 1.00760, "attn_mla_tc.cu"),   # mla_attn_kernel_mla32_full.md
     "gqa": ("de022da015e73ab4", 1.00383, "attn_gqa_tc.cu"),   # gqa_attn_kernel_qwen_full.md
 }
 

@@ -403,7 +403,6 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
     // waits and the abort flag are made warp-uniform: the tcgen05 ld/st below
     // are .sync.aligned and need every lane
     auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
-      if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
       return __all_sync(0xffffffffu, mbar_wait(bar, par, kWaitNs));
     };
     // One-tile lookahead: tile t+1's partial scores are read out of TMEM (and
@@ -423,6 +422,7 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
     };
     if (T > 0 && !load_scores(0)) ok = false;
     for (int t = 0; t < T && ok; ++t) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
       float x[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) x[k] = nx[k];
