@@ -538,6 +538,7 @@ def run_reference(args):
     if torch.cuda.is_available():
         torch.cuda.set_device(0)
     inst = setup_reference_inputs(w)
+    alg = algorithmic(w, inst.seq_lens.cpu().numpy())
     budget = max(2.0, args.cpu_budget / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_time(inst, budget, args.cpu_max_seqs)
@@ -556,7 +557,11 @@ def run_reference(args):
         "ms_per_step": round(secs / args.steps * 1e3, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "kind": w.kind, "batch": w.batch, "q_len": w.q_len,
-                   "dcp_size": w.dcp_size, "interleave": w.interleave},
+                   "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+                   "head_dim_qk": w.head_dim_qk, "head_dim_v": w.head_dim_v,
+                   "block_size": w.block_size, "dcp_size": w.dcp_size, "interleave": w.interleave,
+                   "kv_tokens": alg["tokens"], "kv_bytes": alg["kv_bytes"],
+                   "l2": "not applicable (host oracle)", "parallelism": "host cores (numpy)"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cpu_threads(),
                          "kind": "oracle", "cpu_count": os.cpu_count(),
                          "omp_num_threads": os.environ.get("OMP_NUM_THREADS"),
