@@ -76,3 +76,10 @@ def test_reference_arm_rank0_only_under_torchrun():
     assert rec["unit"] == "GB/s" and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle"
     assert rec["e2e"]["h2d_bytes_per_step"] == 0
+    # the same workload description as the GPU arm's line
+    cfg = rec["config"]
+    for key in ("workload", "kind", "batch", "q_len", "num_q_heads", "num_kv_heads", "head_dim_qk",
+                "head_dim_v", "block_size", "dcp_size", "interleave", "kv_tokens", "kv_bytes"):
+        assert key in cfg, key
+    assert cfg["workload"] == "tiny_gqa" and cfg["kv_tokens"] == 1024
+    assert rec["higher_is_better"] is True and rec["steps"] == 1
