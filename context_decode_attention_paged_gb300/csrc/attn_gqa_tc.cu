@@ -15,6 +15,11 @@
 //                   K tile K-major and Q^T K-major, both 128B-swizzled smem)
 //   O^T += V^T P^T (M = 128 value dims, N = NCOL, K = 128 keys;
 //                   V tile read MN-major from the same stage, P^T MN-major smem)
+// P carries two bf16 terms, P_hi = bf16(p) and P_lo = bf16(p - P_hi), each with
+// its own PV product into the same accumulator: p keeps 16 significant bits
+// instead of 8, so a few dominant keys whose values nearly cancel do not leave
+// the 2^-9 rounding of their probabilities in the output.  The tensor pipe has
+// the room (this kernel is bound by HBM at 16 flop per cache byte).
 // NCOL is 16, 32 or 64 (the tile's query rows, padded); longer causal queries
 // (chunked prefill) take several row tiles, each streaming the shard's keys.
 // K and V tiles of 128 tokens stream through a TMA ring; a 3-D tensor map over
@@ -56,7 +61,6 @@ constexpr int kFirstSoftWarp = 3;             // warps 3.. : softmax
 constexpr int kSoftGroups = 4;                 // softmax warps per TMEM lane quadrant
 constexpr uint32_t kSoftThreads = 128 * kSoftGroups;
 constexpr uint32_t kThreads = 96 + kSoftThreads;
-constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxCols = 64;                   // query rows per row tile
 constexpr size_t kSmemLimit = 232448;          // dynamic shared memory per CTA
@@ -75,6 +79,8 @@ struct GqaParams {
   int D;               // head dim (64 or 128)
   int stages;
   float scale_log2;
+  unsigned long long wait_ns;   // limit of every bounded wait
+  int skip_tile;                // test hook: the producer never loads this tile (-1: off)
 };
 
 struct Smem {
@@ -107,7 +113,7 @@ struct Cfg {
 };
 
 __host__ __device__ constexpr size_t gqa_fixed_bytes(int D, int ncol) {
-  return 1024 + (size_t)(D / 64) * ncol * 128 + 2 * (size_t)kNt * ncol * 2 + sizeof(Smem) + 64;
+  return 1024 + (size_t)(D / 64) * ncol * 128 + 4 * (size_t)kNt * ncol * 2 + sizeof(Smem) + 64;
 }
 
 size_t gqa_stage_bytes(int D) { return 2 * (size_t)(D / 64) * kChunkBytes; }
@@ -171,7 +177,7 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
   for (int t = 0; t < T; ++t) {
     const int bsel = t & 1;
     const bool okw = __all_sync(0xffffffffu, *abort_flag == 0 &&
-                                                 mbar_wait(smem_u32(&sm.s_full[bsel]), (uint32_t)(t >> 1) & 1u, kWaitNs));
+                                                 mbar_wait(smem_u32(&sm.s_full[bsel]), (uint32_t)(t >> 1) & 1u, p.wait_ns));
     if (!okw) bad = true;
     float x[HC];
     {
@@ -226,7 +232,7 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
       // P^T buffer's barrier is at most one phase ahead of what this thread
       // last waited for there (PV(t-3)), so the parity is unambiguous.
       if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_free[(t - 1) & 1]),
-                                                      (uint32_t)((t - 1) >> 1) & 1u, kWaitNs)))
+                                                      (uint32_t)((t - 1) >> 1) & 1u, p.wait_ns)))
         bad = true;
       if (bar_red_or(kBarSoftmax, kSoftThreads, bad)) {
         broke = true;
@@ -254,39 +260,42 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
       }
     }
 
-    // this key's probabilities for this warp's rows -> its half of the P^T row (bf16)
-    uint32_t pk[HC / 2];
-    if (full) {
+    // this key's probabilities for this warp's rows -> its part of the P^T
+    // row, as two bf16 terms (hi, and the remainder lo)
+    uint32_t pk[HC / 2], pl[HC / 2];
 #pragma unroll
-      for (int h = 0; h < HC; h += 2) {
-        const float p0 = ex2(x[h] - m[h]), p1 = ex2(x[h + 1] - m[h + 1]);
-        l[h] += p0;
-        l[h + 1] += p1;
-        pk[h / 2] = pack_bf16x2(p0, p1);
+    for (int h = 0; h < HC; h += 2) {
+      float p0, p1;
+      if (full) {
+        p0 = ex2(x[h] - m[h]);
+        p1 = ex2(x[h + 1] - m[h + 1]);
+      } else {
+        p0 = x[h] == -INFINITY ? 0.f : ex2(x[h] - m[h]);
+        p1 = x[h + 1] == -INFINITY ? 0.f : ex2(x[h + 1] - m[h + 1]);
       }
-    } else {
-#pragma unroll
-      for (int h = 0; h < HC; h += 2) {
-        const float p0 = x[h] == -INFINITY ? 0.f : ex2(x[h] - m[h]);
-        const float p1 = x[h + 1] == -INFINITY ? 0.f : ex2(x[h + 1] - m[h + 1]);
-        l[h] += p0;
-        l[h + 1] += p1;
-        pk[h / 2] = pack_bf16x2(p0, p1);
-      }
+      l[h] += p0;
+      l[h + 1] += p1;
+      const uint32_t hi = pack_bf16x2(p0, p1);
+      pk[h / 2] = hi;
+      pl[h / 2] = pack_bf16x2(p0 - bf16_lo(hi), p1 - bf16_hi(hi));
     }
     if (t >= 2 &&
-        !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_free[bsel]), (uint32_t)((t >> 1) - 1) & 1u, kWaitNs)))
+        !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_free[bsel]), (uint32_t)((t >> 1) - 1) & 1u, p.wait_ns)))
       bad = true;
     uint8_t* prow = ps + bsel * C::kPBytes + lrow * C::kPitch;
+    uint8_t* lrow_p = prow + 2 * C::kPBytes;              // the lo term's buffer
     if constexpr (HC == 4) {
       // half of a 16-byte chunk: the swizzle moves whole chunks
-      *reinterpret_cast<uint2*>(prow + (C::pchunk((uint32_t)(h0 / 8), (uint32_t)lrow) << 4) + (h0 % 8) * 2) =
-          make_uint2(pk[0], pk[1]);
+      const uint32_t off = (C::pchunk((uint32_t)(h0 / 8), (uint32_t)lrow) << 4) + (h0 % 8) * 2;
+      *reinterpret_cast<uint2*>(prow + off) = make_uint2(pk[0], pk[1]);
+      *reinterpret_cast<uint2*>(lrow_p + off) = make_uint2(pl[0], pl[1]);
     } else {
 #pragma unroll
-      for (int c = 0; c < HC / 8; ++c)
-        *reinterpret_cast<uint4*>(prow + (C::pchunk((uint32_t)(h0 / 8 + c), (uint32_t)lrow) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      for (int c = 0; c < HC / 8; ++c) {
+        const uint32_t off = C::pchunk((uint32_t)(h0 / 8 + c), (uint32_t)lrow) << 4;
+        *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        *reinterpret_cast<uint4*>(lrow_p + off) = make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
+      }
     }
     if (h0 == 0 && jj >= ke) {
       // key past the range (ragged last tile): zero its value row so that
@@ -306,7 +315,7 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
   // the last PV (its commit also covers every earlier MMA of the issuer)
   bool have = T > 0 && !broke;
   if (have && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_free[(T - 1) & 1]),
-                                                 (uint32_t)((T - 1) >> 1) & 1u, kWaitNs)))
+                                                 (uint32_t)((T - 1) >> 1) & 1u, p.wait_ns)))
     bad = true;
   if (bar_red_or(kBarSoftmax, kSoftThreads, bad)) have = false;
   if (bad) fail();
@@ -355,8 +364,8 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   const uint32_t stage_bytes = 2u * nch * kChunkBytes;    // V chunks, then K chunks
   uint8_t* stages = base;
   uint8_t* qs = stages + p.stages * stage_bytes;          // Q^T: nch chunks of NCOL rows x 128 B
-  uint8_t* ps = qs + nch * NCOL * 128;                    // two P^T buffers
-  Smem& sm = *reinterpret_cast<Smem*>(ps + 2 * C::kPBytes);
+  uint8_t* ps = qs + nch * NCOL * 128;                    // P^T buffers: hi 0, hi 1, lo 0, lo 1
+  Smem& sm = *reinterpret_cast<Smem*>(ps + 4 * C::kPBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Units in longest-request-first order: the block scheduler starts CTAs in
@@ -398,10 +407,23 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   const int vis = bad_len ? 0 : min(L, local_count_upto((long long)S - p.Lq + i_last, r, p.I, p.N));
   const int kb = min(vis, s_idx * p.split_tokens);
   const int ke = min(vis, kb + p.split_tokens);
-  const int T = (ke - kb + kNt - 1) / kNt;
+  int T = (ke - kb + kNt - 1) / kNt;
   // keys below lim_min are visible to every row of the tile
   const int lim_min = bad_len ? 0 : min(ke, local_count_upto((long long)S - p.Lq + i_first, r, p.I, p.N));
   if (tid == 0 && (bad_len || short_table)) set_status(p.status, DCP_ERR_BOUNDS);
+  {
+    // a block id past the pool among the tile's visible keys skips the unit
+    // (every KV split of it: zero partial, -inf LSE) and reports
+    // DCP_ERR_BOUNDS; table entries past the key range are never read
+    const int32_t* bt = p.block_tables + ((long long)r * p.B + b) * p.max_lb;
+    bool bad_blk = false;
+    for (int jb = tid; jb < (vis + p.bs - 1) / p.bs; jb += (int)kThreads)
+      bad_blk |= (unsigned)bt[jb] >= (unsigned)p.num_blocks;
+    if (__syncthreads_or(bad_blk)) {
+      T = 0;
+      if (tid == 0) set_status(p.status, DCP_ERR_BOUNDS);
+    }
+  }
 
   if (tid == 0) {
     for (int k = 0; k < p.stages; ++k) {
@@ -464,21 +486,21 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       for (int t = 0; t < T; ++t) {
         const int st = t % p.stages;
         const uint32_t ph = (uint32_t)(t / p.stages) & 1u;
-        if (*abort_flag || !mbar_wait(smem_u32(&sm.kv_empty[st]), ph ^ 1u, kWaitNs)) {
+        if (*abort_flag || !mbar_wait(smem_u32(&sm.kv_empty[st]), ph ^ 1u, p.wait_ns)) {
           fail();
           break;
         }
+        // test hook: this tile is never loaded, so the bounded waits on it run
+        // out and the unit unwinds
+        if (t == p.skip_tile) continue;
         const uint32_t full = smem_u32(&sm.kv_full[st]);
         uint8_t* dst = stages + st * stage_bytes;
         mbar_arrive_expect_tx(full, stage_bytes);
         for (int k = 0; k < boxes; ++k) {
           const int j = kb + t * kNt + k * box_rows;
-          // boxes past the last block of the table read block 0's slot (zeros
-          // or stale rows are masked); in-range j always has a table entry
-          const int jb = j / p.bs;
-          const int blk = jb < p.max_lb ? bt[jb] : 0;
-          if ((unsigned)blk >= (unsigned)p.num_blocks) set_status(p.status, DCP_ERR_BOUNDS);
-          const int row = blk * p.bs + (j % p.bs);       // out-of-range rows read as zeros
+          // boxes past the key range read pool row 0 (masked, values zeroed);
+          // the others' block ids were checked against the pool above
+          const int row = j < ke ? bt[j / p.bs] * p.bs + (j % p.bs) : 0;
           for (int c = 0; c < nch; ++c) {
             tma_load_3d(smem_u32(dst + c * kChunkBytes + k * box_rows * 128), &tm_v, 64 * c, g, row, full);
             tma_load_3d(smem_u32(dst + (nch + c) * kChunkBytes + k * box_rows * 128), &tm_k, 64 * c, g, row,
@@ -489,7 +511,7 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       }
       if (*abort_flag) {
         for (int k = 0; k < p.stages; ++k)
-          if (issued[k] > 0) mbar_wait(smem_u32(&sm.kv_full[k]), (uint32_t)(issued[k] - 1) & 1u, kWaitNs);
+          if (issued[k] > 0) mbar_wait(smem_u32(&sm.kv_full[k]), (uint32_t)(issued[k] - 1) & 1u, p.wait_ns);
       }
     }
   } else if (warp == 1) {
@@ -507,8 +529,8 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       for (int t = 0; t < T; ++t) {
         const int st = t % p.stages;
         if (*abort_flag ||
-            !mbar_wait(smem_u32(&sm.kv_full[st]), (uint32_t)(t / p.stages) & 1u, kWaitNs) ||
-            (t >= 2 && !mbar_wait(smem_u32(&sm.s_free[t & 1]), (uint32_t)((t >> 1) - 1) & 1u, kWaitNs))) {
+            !mbar_wait(smem_u32(&sm.kv_full[st]), (uint32_t)(t / p.stages) & 1u, p.wait_ns) ||
+            (t >= 2 && !mbar_wait(smem_u32(&sm.s_free[t & 1]), (uint32_t)((t >> 1) - 1) & 1u, p.wait_ns))) {
           ok = false;
           break;
         }
@@ -526,7 +548,7 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       }
       if (!ok) fail();
       mma_commit(smem_u32(&sm.drain[0]));
-      if (!mbar_wait(smem_u32(&sm.drain[0]), 0, kWaitNs)) fail();
+      if (!mbar_wait(smem_u32(&sm.drain[0]), 0, p.wait_ns)) fail();
     }
   } else if (warp == 2) {
     // ---------------- PV issuer: O^T += V^T(t) P^T(t) ----------------
@@ -536,7 +558,7 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
       // A = V^T (dims x keys) read MN-major from the value chunks; B = P^T
       bool ok = true;
       for (int t = 0; t < T; ++t) {
-        if (*abort_flag || !mbar_wait(smem_u32(&sm.p_full[t & 1]), (uint32_t)(t >> 1) & 1u, kWaitNs)) {
+        if (*abort_flag || !mbar_wait(smem_u32(&sm.p_full[t & 1]), (uint32_t)(t >> 1) & 1u, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -546,15 +568,18 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         // 8-row swizzle atoms (2048 B of V, 8 rows of P^T) to the start address
         const uint64_t dv = smem_desc(smem_u32(stages + st * stage_bytes), kChunkBytes, 1024, kSw128);
         const uint64_t dp = smem_desc(smem_u32(ps + (t & 1) * C::kPBytes), C::kPBytes, 8 * C::kPitch, C::kPSwz);
+        const uint64_t dpl = smem_desc(smem_u32(ps + (2 + (t & 1)) * C::kPBytes), C::kPBytes, 8 * C::kPitch, C::kPSwz);
 #pragma unroll
-        for (uint32_t k = 0; k < kNt / 16; ++k)
+        for (uint32_t k = 0; k < kNt / 16; ++k) {
           mma_ss(tO, dv + ((k * 2048u) >> 4), dp + ((k * 16u * C::kPitch) >> 4), id_pv, (t > 0 || k > 0) ? 1u : 0u);
+          mma_ss(tO, dv + ((k * 2048u) >> 4), dpl + ((k * 16u * C::kPitch) >> 4), id_pv, 1u);
+        }
         mma_commit(smem_u32(&sm.p_free[t & 1]));
         mma_commit(smem_u32(&sm.kv_empty[st]));
       }
       if (!ok) fail();
       mma_commit(smem_u32(&sm.drain[1]));
-      if (!mbar_wait(smem_u32(&sm.drain[1]), 0, kWaitNs)) fail();
+      if (!mbar_wait(smem_u32(&sm.drain[1]), 0, p.wait_ns)) fail();
     }
   } else {
     softmax_epilogue<NCOL>(p, sm, stages, stage_bytes, ps, tmem, warp, lane, T, kb, ke, lim_min, R, row0,
@@ -637,6 +662,8 @@ cudaError_t launch_attn_gqa_tc(const AttnArgs& a, const SplitPlan& plan) {
   p.D = a.Dqk;
   p.stages = gqa_stages(a.Dqk, ncol);
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.wait_ns = test_hooks().wait_ns;
+  p.skip_tile = test_hooks().skip_tile;
   if (plan.n_split > 1) {
     const size_t nrows = (size_t)a.N * a.B * a.Lq * a.Hq;
     const size_t o_bytes = nrows * plan.n_split * a.Dv * sizeof(float);

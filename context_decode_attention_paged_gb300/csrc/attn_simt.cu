@@ -60,7 +60,19 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(SimtParams P) {
     L = a.max_lb * a.bs;
   }
   const int j_begin = min(L, s * P.split_tokens);
-  const int j_end = min(L, j_begin + P.split_tokens);
+  int j_end = min(L, j_begin + P.split_tokens);
+  {
+    // a block id past the pool among the shard's keys skips the unit (every KV
+    // split of it: zero partial, -inf LSE) and reports DCP_ERR_BOUNDS
+    const int* btr = a.block_tables + ((long long)r * a.B + b) * a.max_lb;
+    bool bad_blk = false;
+    for (int jb = tid; jb < (L + a.bs - 1) / a.bs; jb += kThreads)
+      bad_blk |= (unsigned)btr[jb] >= (unsigned)a.num_blocks;
+    if (__syncthreads_or(bad_blk)) {
+      j_end = j_begin;
+      if (tid == 0) set_status(a.status, DCP_ERR_BOUNDS);
+    }
+  }
 
   // query rows -> smem (fp32), per-row visible-key limits
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
@@ -98,11 +110,7 @@ __global__ void __launch_bounds__(kThreads) attn_simt_kernel(SimtParams P) {
       float kval = 0.f, vval = 0.f;
       if (tt < nt) {
         const int j = j0 + tt;
-        int blk = bt[j / a.bs];
-        if (blk < 0 || blk >= a.num_blocks) {
-          set_status(a.status, DCP_ERR_BOUNDS);
-          blk = 0;
-        }
+        const int blk = bt[j / a.bs];                 // checked against the pool above
         const long long off = (((long long)blk * a.bs + j % a.bs) * a.Hkv + g) * a.Dqk + d;
         kval = __bfloat162float(kv[off]);
         if (a.kind == DCP_ATTN_GQA && d < a.Dv) vval = __bfloat162float(kv[pool_elems + off]);

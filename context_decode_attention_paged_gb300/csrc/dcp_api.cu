@@ -4,6 +4,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "dcp_internal.h"
 
@@ -90,6 +91,16 @@ SplitPlan plan_for(const AttnArgs& a, Impl impl, int sm_count) {
 }
 
 }  // namespace
+
+namespace {
+std::mutex g_hooks_mu;
+TestHooks g_hooks = {2000000000ull, -1};
+}  // namespace
+
+TestHooks test_hooks() {
+  std::lock_guard<std::mutex> lock(g_hooks_mu);
+  return g_hooks;
+}
 
 int device_sm_count() {
   int dev = 0, n = 0;
@@ -255,6 +266,13 @@ dcp_status_t dcp_merge(const float* partial_out, const float* lse, int32_t dcp_s
     return DCP_ERR_INVALID_ARG;
   return from_cuda(launch_merge(partial_out, lse, dcp_size, batch, q_len, num_q_heads,
                                 head_dim_v, out, out_lse, static_cast<cudaStream_t>(stream)));
+}
+
+// Test-only (see TestHooks in dcp_internal.h); not declared in include/dcp.h.
+DCP_API void dcp_testing_set_hooks(unsigned long long wait_ns, int32_t skip_tile) {
+  std::lock_guard<std::mutex> lock(g_hooks_mu);
+  g_hooks.wait_ns = wait_ns > 0 ? wait_ns : 2000000000ull;
+  g_hooks.skip_tile = skip_tile;
 }
 
 dcp_status_t dcp_get_last_device_status(void* stream) {

@@ -41,6 +41,18 @@ SplitPlan plan_splits(const AttnArgs& a, int sm_count, int tile_tokens, int unit
 
 int device_sm_count();
 
+// Test-only knobs of the attention kernels, read at each launch: the limit of
+// every bounded wait (default 2 s) and a tile that the first CTA's TMA
+// producer of every work unit never loads (-1: none), so that the kernels'
+// own bounded waits run out and their abort paths run.  Set through
+// dcp_testing_set_hooks, an exported symbol the public header does not
+// declare; nothing in the library changes them.
+struct TestHooks {
+  unsigned long long wait_ns;
+  int skip_tile;
+};
+TestHooks test_hooks();
+
 // Launchers; each returns a cudaError_t from the launch.
 cudaError_t launch_slot_map(const int32_t* seq_lens, int B, int bs, int I, int N,
                             int32_t* local_seq_lens, int32_t* local_num_blocks,

@@ -57,6 +57,12 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
                :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar) : "memory");
 }
 
+// 8-byte variant of st_async_v4.
+__device__ __forceinline__ void st_async_v2(uint32_t addr, float a, float b, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+               :: "r"(addr), "f"(a), "f"(b), "r"(cluster_bar) : "memory");
+}
+
 // 4-byte variant of st_async_v4.
 __device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t cluster_bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
