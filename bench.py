@@ -74,13 +74,13 @@ def algorithmic(w: wl.Workload, seq_lens) -> dict:
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one attention
-# launch, as a multiple of its algorithmic bytes, from the ncu captures
-# summarised in profiles/ (a smaller case of the same kernel; traffic scales
-# with the cache bytes processed).  Keyed by the kernel source the counters
-# were taken on: once the source changes, traffic is reported as null.
+# launch, as a multiple of its algorithmic bytes, from an ncu capture of a
+# smaller case of the same kernel (traffic scales with the cache bytes
+# processed).  Keyed by the kernel source the counters were taken on: once the
+# source changes, traffic is reported as null.
 NCU_TRAFFIC_RATIO = {
-    "mla": ("72df035987125067", 1.00760, "attn_mla_tc.cu"),   # mla_attn_kernel_mla32_full.md
-    "gqa": ("de022da015e73ab4", 1.00383, "attn_gqa_tc.cu"),   # gqa_attn_kernel_qwen_full.md
+    "mla": ("72df035987125067", 1.00760, "attn_mla_tc.cu"),
+    "gqa": ("de022da015e73ab4", 1.00383, "attn_gqa_tc.cu"),
 }
 
 
@@ -328,6 +328,79 @@ def cpu_threads() -> int:
 # main legs
 # ---------------------------------------------------------------------------
 
+# The other workload configurations, measured in the same run after the headline
+# one and reported beside it (single GPU).
+OTHER_CONFIGS = ("tiny_gqa", "qwen_gqa", "mla_32", "mla_mtp")
+
+
+def roofline_of(w, alg, attn_ms: float, peaks) -> dict:
+    """Roofline record of the attention launch: HBM when its algorithmic bytes at
+    the copy rate take longer than its flops at the bf16 rate, else tensor."""
+    hbm = float(peaks["hbm_gbs"])
+    tflops = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    gbs = alg["attn_bytes"] / (attn_ms * 1e-3) / 1e9
+    tfs = alg["flops"] / (attn_ms * 1e-3) / 1e12
+    if alg["attn_bytes"] / hbm >= alg["flops"] / (tflops * 1e3):
+        return {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4)}
+    return {"bound": "tensor", "achieved": round(tfs, 1), "peak": tflops, "unit": "TFLOP/s",
+            "frac": round(tfs / tflops, 4)}
+
+
+def measure_config(name: str, steps: int, warmup: int, dev, peaks) -> dict:
+    """One workload configuration, timed like the headline one: attention +
+    merge per step, CUDA events on the launching stream, L2 flushed before each
+    step when the cache is small enough to stay in it."""
+    from context_decode_attention_paged_gb300 import binding as dcp
+    w = wl.WORKLOADS[name]
+    inst = setup_gpu(w, 0)
+    N, B, Lq, Hq, Dv = w.dcp_size, w.batch, w.q_len, w.num_q_heads, w.head_dim_v
+    po = torch.empty((N, B, Lq, Hq, Dv), dtype=torch.float32, device=dev)
+    lse = torch.empty((N, B, Lq, Hq), dtype=torch.float32, device=dev)
+    out = torch.empty((N, B, Lq, Hq // N, Dv), dtype=torch.bfloat16, device=dev)
+    out_lse = torch.empty((N, B, Lq, Hq // N), dtype=torch.float32, device=dev)
+    desc = dcp.desc_from_tensors(w.kind, inst.q, inst.kv_cache, inst.block_tables, Dv)
+    ws_bytes = dcp.dcp_decode_attn_workspace_size(desc, N)
+    ws = torch.empty((max(ws_bytes, 1),), dtype=torch.uint8, device=dev) if ws_bytes else None
+    attn, merge = step_fn(inst, po, lse, out, out_lse, ws)
+    alg = algorithmic(w, inst.seq_lens.cpu().numpy())
+    for _ in range(warmup):
+        attn()
+        merge()
+    torch.cuda.synchronize()
+    flush = alg["kv_bytes"] <= L2_FLUSH_BELOW
+    scratch = torch.empty((1 << 30,), dtype=torch.uint8, device=dev) if flush else None
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for k in range(steps):
+        if flush:
+            scratch.fill_(k & 0xFF)
+        ev[k][0].record(stream)
+        attn()
+        ev[k][1].record(stream)
+        merge()
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    st = dcp.dcp_get_last_device_status()
+    if st != dcp.DCP_OK:
+        raise RuntimeError(f"{name}: device status {dcp.status_string(st)}")
+    attn_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    step_ms = statistics.mean(e[0].elapsed_time(e[2]) for e in ev)
+    attn_avg = statistics.mean(attn_ms)
+    rec = {"workload": name, "kind": w.kind, "batch": B, "q_len": Lq, "dcp_size": N,
+           "interleave": w.interleave, "kv_tokens": alg["tokens"], "kv_bytes": alg["kv_bytes"],
+           "step_ms": round(step_ms, 4), "kv_gbs": round(alg["kv_bytes"] / (step_ms * 1e-3) / 1e9, 2),
+           "query_tokens_per_s": round(B * Lq / (step_ms * 1e-3), 1),
+           "attn_ms": round(attn_avg, 4), "attn_ms_median": round(statistics.median(attn_ms), 4),
+           "alg_bytes_per_launch": alg["attn_bytes"], "alg_flops_per_launch": alg["flops"],
+           "roofline": roofline_of(w, alg, attn_avg, peaks),
+           "l2": "L2 flushed before each timed step (1 GB write, untimed)" if flush
+           else "inputs larger than L2 (cache resident, no flush)",
+           "steps": steps, "warmup": warmup}
+    del inst, po, lse, out, out_lse, ws, scratch
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_ours(args):
     world, rank, local = dist_env()
     if world > 1:
@@ -513,6 +586,12 @@ def run_ours(args):
         "gpu_launches": launches_per_step * args.steps,
         "kv_write": kv_write,
     }
+    if world == 1 and not args.no_other_configs:
+        others = {}
+        for name in OTHER_CONFIGS:
+            if name != w.name:
+                others[name] = measure_config(name, args.steps, args.warmup, dev, peaks)
+        result["configs"] = others
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         secs, kvb, nseq, qtok = oracle_time(inst, args.cpu_budget, args.cpu_max_seqs)
         result["cpu_baseline"] = {
@@ -595,6 +674,8 @@ def main():
                     help="seconds of oracle time for the CPU baseline sample")
     ap.add_argument("--cpu-max-seqs", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="measure only the named workload (the other configurations are reported by default)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

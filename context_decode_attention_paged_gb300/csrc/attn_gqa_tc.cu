@@ -15,11 +15,12 @@
 //                   K tile K-major and Q^T K-major, both 128B-swizzled smem)
 //   O^T += V^T P^T (M = 128 value dims, N = NCOL, K = 128 keys;
 //                   V tile read MN-major from the same stage, P^T MN-major smem)
-// P carries two bf16 terms, P_hi = bf16(p) and P_lo = bf16(p - P_hi), each with
-// its own PV product into the same accumulator: p keeps 16 significant bits
-// instead of 8, so a few dominant keys whose values nearly cancel do not leave
-// the 2^-9 rounding of their probabilities in the output.  The tensor pipe has
-// the room (this kernel is bound by HBM at 16 flop per cache byte).
+// P carries two bf16 terms, P_hi = bf16(p) and P_lo = bf16(p - P_hi): p keeps
+// 16 significant bits instead of 8, so a few dominant keys whose values nearly
+// cancel do not leave the 2^-9 rounding of their probabilities in the output.
+// The two P^T buffers of a tile sit one swizzle atom apart, so one PV MMA with
+// N = 2 NCOL accumulates O_hi^T and O_lo^T side by side; the epilogue adds
+// them.  The MMA count per tile stays that of one term.
 // NCOL is 16, 32 or 64 (the tile's query rows, padded); longer causal queries
 // (chunked prefill) take several row tiles, each streaming the shard's keys.
 // K and V tiles of 128 tokens stream through a TMA ring; a 3-D tensor map over
@@ -144,7 +145,7 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
   const int h0 = ((warp - kFirstSoftWarp) >> 2) * HC;     // first column of this warp
   const int lrow = qd * 32 + lane;
   const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
-  const uint32_t tO = lane_base + 2 * NCOL + h0;
+  const uint32_t tO = lane_base + 2 * NCOL + h0;         // O_hi^T; O_lo^T is NCOL columns on
   volatile int* abort_flag = &sm.abort;
   float m[HC], l[HC];
 #pragma unroll
@@ -250,12 +251,15 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
       }
       if (t > 0) {
         tc_fence_after();
-        uint32_t o[HC];
-        ld_cols(tO, o);
-        tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < HC; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha[k]);
-        st_cols(tO, o);
+        for (int part = 0; part < 2; ++part) {
+          uint32_t o[HC];
+          ld_cols(tO + part * NCOL, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < HC; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha[k]);
+          st_cols(tO + part * NCOL, o);
+        }
         tmem_wait_st();
       }
     }
@@ -282,8 +286,8 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
     if (t >= 2 &&
         !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_free[bsel]), (uint32_t)((t >> 1) - 1) & 1u, p.wait_ns)))
       bad = true;
-    uint8_t* prow = ps + bsel * C::kPBytes + lrow * C::kPitch;
-    uint8_t* lrow_p = prow + 2 * C::kPBytes;              // the lo term's buffer
+    uint8_t* prow = ps + 2 * bsel * C::kPBytes + lrow * C::kPitch;
+    uint8_t* lrow_p = prow + C::kPBytes;                  // the lo term's buffer, one atom on
     if constexpr (HC == 4) {
       // half of a 16-byte chunk: the swizzle moves whole chunks
       const uint32_t off = (C::pchunk((uint32_t)(h0 / 8), (uint32_t)lrow) << 4) + (h0 % 8) * 2;
@@ -336,8 +340,12 @@ __device__ __forceinline__ void softmax_epilogue(const GqaParams& p, Smem& sm, u
   for (int h = 0; h < HC; ++h) o[h] = 0u;
   if (have) {
     tc_fence_after();
+    uint32_t olo[HC];
     ld_cols(tO, o);
+    ld_cols(tO + NCOL, olo);
     tmem_wait_ld();
+#pragma unroll
+    for (int h = 0; h < HC; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) + __uint_as_float(olo[h]));
   }
 #pragma unroll
   for (int h = 0; h < HC; ++h) {
@@ -364,7 +372,7 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   const uint32_t stage_bytes = 2u * nch * kChunkBytes;    // V chunks, then K chunks
   uint8_t* stages = base;
   uint8_t* qs = stages + p.stages * stage_bytes;          // Q^T: nch chunks of NCOL rows x 128 B
-  uint8_t* ps = qs + nch * NCOL * 128;                    // P^T buffers: hi 0, hi 1, lo 0, lo 1
+  uint8_t* ps = qs + nch * NCOL * 128;                    // P^T buffers: hi 0, lo 0, hi 1, lo 1
   Smem& sm = *reinterpret_cast<Smem*>(ps + 4 * C::kPBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -553,7 +561,7 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
   } else if (warp == 2) {
     // ---------------- PV issuer: O^T += V^T(t) P^T(t) ----------------
     if (lane == 0 && T > 0) {
-      constexpr uint32_t id_pv = idesc_bf16_ab(128, NCOL, true, true);
+      constexpr uint32_t id_pv = idesc_bf16_ab(128, 2 * NCOL, true, true);   // [P_hi | P_lo]
       const uint32_t tO = tmem + 2 * NCOL;
       // A = V^T (dims x keys) read MN-major from the value chunks; B = P^T
       bool ok = true;
@@ -567,13 +575,11 @@ gqa_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         // base descriptors of this stage and P^T buffer; the K-steps add whole
         // 8-row swizzle atoms (2048 B of V, 8 rows of P^T) to the start address
         const uint64_t dv = smem_desc(smem_u32(stages + st * stage_bytes), kChunkBytes, 1024, kSw128);
-        const uint64_t dp = smem_desc(smem_u32(ps + (t & 1) * C::kPBytes), C::kPBytes, 8 * C::kPitch, C::kPSwz);
-        const uint64_t dpl = smem_desc(smem_u32(ps + (2 + (t & 1)) * C::kPBytes), C::kPBytes, 8 * C::kPitch, C::kPSwz);
+        // the hi and lo buffers are the two N atoms of one operand (LBO = one buffer)
+        const uint64_t dp = smem_desc(smem_u32(ps + 2 * (t & 1) * C::kPBytes), C::kPBytes, 8 * C::kPitch, C::kPSwz);
 #pragma unroll
-        for (uint32_t k = 0; k < kNt / 16; ++k) {
+        for (uint32_t k = 0; k < kNt / 16; ++k)
           mma_ss(tO, dv + ((k * 2048u) >> 4), dp + ((k * 16u * C::kPitch) >> 4), id_pv, (t > 0 || k > 0) ? 1u : 0u);
-          mma_ss(tO, dv + ((k * 2048u) >> 4), dpl + ((k * 16u * C::kPitch) >> 4), id_pv, 1u);
-        }
         mma_commit(smem_u32(&sm.p_free[t & 1]));
         mma_commit(smem_u32(&sm.kv_empty[st]));
       }
