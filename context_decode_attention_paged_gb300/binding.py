@@ -27,6 +27,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 DCP_OK, DCP_ERR_INVALID_ARG, DCP_ERR_UNSUPPORTED, DCP_ERR_CUDA, DCP_ERR_TIMEOUT, DCP_ERR_BOUNDS = range(6)
 DCP_ATTN_GQA, DCP_ATTN_MLA = 0, 1
+DCP_KERNEL_NONE, DCP_KERNEL_MLA_TC, DCP_KERNEL_GQA_TC, DCP_KERNEL_SIMT = range(4)
 KINDS = {"gqa": DCP_ATTN_GQA, "mla": DCP_ATTN_MLA}
 
 
@@ -52,6 +53,8 @@ _lib.dcp_kv_cache_write.argtypes = [ctypes.POINTER(DcpAttnDesc), _vp, _vp, _vp, 
                                     _i32, _vp]
 _lib.dcp_merge.restype = _i32
 _lib.dcp_merge.argtypes = [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]
+_lib.dcp_decode_attn_kernel_kind.restype = _i32
+_lib.dcp_decode_attn_kernel_kind.argtypes = [ctypes.POINTER(DcpAttnDesc), _i32]
 _lib.dcp_get_last_device_status.restype = _i32
 _lib.dcp_get_last_device_status.argtypes = [_vp]
 _lib.dcp_status_string.restype = ctypes.c_char_p
@@ -117,6 +120,11 @@ def dcp_build_slot_map(seq_lens, block_size, interleave, dcp_size, max_seq=None,
 
 def dcp_decode_attn_workspace_size(desc: DcpAttnDesc, dcp_size: int) -> int:
     return int(_lib.dcp_decode_attn_workspace_size(ctypes.byref(desc), dcp_size))
+
+
+def dcp_decode_attn_kernel_kind(desc: DcpAttnDesc, dcp_size: int) -> int:
+    """Which kernel dcp_decode_attn runs for this shape (DCP_KERNEL_*)."""
+    return int(_lib.dcp_decode_attn_kernel_kind(ctypes.byref(desc), dcp_size))
 
 
 def dcp_decode_attn(kind, q, kv_cache, block_tables, seq_lens, dcp_size, interleave, scale,

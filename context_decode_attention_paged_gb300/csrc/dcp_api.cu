@@ -1,10 +1,15 @@
 // C-ABI layer of libdcp: argument checks, split planning, kernel selection,
-// device status word.  Every public entry point is declared in include/dcp.h.
+// the per-stream device status words, NVTX ranges.  Every public entry point
+// is declared in include/dcp.h.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include <algorithm>
+#include <climits>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "dcp_internal.h"
 
@@ -12,21 +17,47 @@ namespace dcp {
 
 namespace {
 
-__device__ int g_status;  // first device-side error since the last read
+// One status word per stream: the first device-side error since that
+// stream's last read.  Streams get their own word in order of first use;
+// once DCP_STATUS_STREAMS - 1 streams of a device have one, further streams
+// share the last word.
+__device__ int g_status[DCP_STATUS_STREAMS];
 
 constexpr int kMaxDevices = 64;
-int* g_status_ptr[kMaxDevices] = {nullptr};
+std::mutex g_status_mu;
+int* g_status_base[kMaxDevices] = {nullptr};
+std::map<std::pair<int, cudaStream_t>, int> g_status_slot;
+int g_status_used[kMaxDevices] = {0};
 
-int* status_ptr() {
+// Device address of the status word of `stream` on the current device (the
+// first use on a device looks up the array's address).
+int* status_ptr(cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!g_status_ptr[dev]) {
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (!g_status_base[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
-    g_status_ptr[dev] = static_cast<int*>(p);
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess || p == nullptr) return nullptr;
+    g_status_base[dev] = static_cast<int*>(p);
   }
-  return g_status_ptr[dev];
+  const auto key = std::make_pair(dev, stream);
+  auto it = g_status_slot.find(key);
+  int slot;
+  if (it != g_status_slot.end()) {
+    slot = it->second;
+  } else {
+    slot = std::min(g_status_used[dev], DCP_STATUS_STREAMS - 1);
+    if (g_status_used[dev] < DCP_STATUS_STREAMS - 1) ++g_status_used[dev];
+    g_status_slot.emplace(key, slot);
+  }
+  return g_status_base[dev] + slot;
 }
+
+// NVTX range around a C-ABI call (no cost unless a profiler is attached)
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -170,13 +201,16 @@ dcp_status_t dcp_build_slot_map(const int32_t* seq_lens, int32_t batch, int32_t 
                                 int32_t interleave, int32_t dcp_size, int32_t* local_seq_lens,
                                 int32_t* local_num_blocks, int32_t* shard_of, int32_t* local_pos,
                                 int32_t max_seq, void* stream) {
+  NvtxRange range("dcp_build_slot_map");
   if (batch < 0 || block_size < 1 || interleave < 1 || dcp_size < 1) return DCP_ERR_INVALID_ARG;
   if (batch > 0 && (!seq_lens || !local_seq_lens || !local_num_blocks)) return DCP_ERR_INVALID_ARG;
   if ((shard_of == nullptr) != (local_pos == nullptr)) return DCP_ERR_INVALID_ARG;
   if (shard_of && max_seq < 1) return DCP_ERR_INVALID_ARG;
   if ((long long)batch * dcp_size > (1LL << 30)) return DCP_ERR_INVALID_ARG;
+  // one thread per (request, token) of the optional maps: the grid must fit
+  if (shard_of && (long long)batch * max_seq > (long long)INT_MAX * 256) return DCP_ERR_INVALID_ARG;
   if (batch == 0) return DCP_OK;
-  int* st = status_ptr();
+  int* st = status_ptr(static_cast<cudaStream_t>(stream));
   if (!st) return DCP_ERR_CUDA;
   return from_cuda(launch_slot_map(seq_lens, batch, block_size, interleave, dcp_size,
                                    local_seq_lens, local_num_blocks, shard_of, local_pos, max_seq,
@@ -194,6 +228,7 @@ dcp_status_t dcp_decode_attn(const dcp_attn_desc_t* d, const void* q, const void
                              int32_t dcp_size, int32_t interleave, float scale,
                              int32_t causal_q_len, float* partial_out, float* lse,
                              void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange range("dcp_decode_attn");
   AttnArgs a{};
   dcp_status_t st = make_args(d, dcp_size, interleave, scale, causal_q_len, &a);
   if (st != DCP_OK) return st;
@@ -214,7 +249,7 @@ dcp_status_t dcp_decode_attn(const dcp_attn_desc_t* d, const void* q, const void
   a.lse = lse;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
-  a.status = status_ptr();
+  a.status = status_ptr(static_cast<cudaStream_t>(stream));
   if (!a.status) return DCP_ERR_CUDA;
   a.stream = static_cast<cudaStream_t>(stream);
   switch (impl) {
@@ -231,6 +266,7 @@ dcp_status_t dcp_decode_attn(const dcp_attn_desc_t* d, const void* q, const void
 dcp_status_t dcp_kv_cache_write(const dcp_attn_desc_t* d, const void* new_k, const void* new_v,
                                 void* kv_cache, const int32_t* block_tables, const int32_t* seq_lens,
                                 int32_t dcp_size, int32_t interleave, int32_t n_new, void* stream) {
+  NvtxRange range("dcp_kv_cache_write");
   if (!d || !new_k || !kv_cache || !block_tables || !seq_lens) return DCP_ERR_INVALID_ARG;
   if (d->kind != DCP_ATTN_GQA && d->kind != DCP_ATTN_MLA) return DCP_ERR_INVALID_ARG;
   const bool gqa = d->kind == DCP_ATTN_GQA;
@@ -246,7 +282,7 @@ dcp_status_t dcp_kv_cache_write(const dcp_attn_desc_t* d, const void* new_k, con
     return DCP_ERR_INVALID_ARG;
   if (!aligned(new_k, 16) || !aligned(kv_cache, 16) || (new_v && !aligned(new_v, 16)))
     return DCP_ERR_INVALID_ARG;
-  int* st = status_ptr();
+  int* st = status_ptr(static_cast<cudaStream_t>(stream));
   if (!st) return DCP_ERR_CUDA;
   return from_cuda(launch_kv_write(new_k, new_v, kv_cache, block_tables, seq_lens, d->batch, n_new, dcp_size,
                                    interleave, d->block_size, d->max_local_blocks, d->num_blocks,
@@ -256,6 +292,7 @@ dcp_status_t dcp_kv_cache_write(const dcp_attn_desc_t* d, const void* new_k, con
 dcp_status_t dcp_merge(const float* partial_out, const float* lse, int32_t dcp_size,
                        int32_t batch, int32_t q_len, int32_t num_q_heads, int32_t head_dim_v,
                        void* out, float* out_lse, void* stream) {
+  NvtxRange range("dcp_merge");
   if (!partial_out || !lse || !out) return DCP_ERR_INVALID_ARG;
   if (dcp_size < 1 || dcp_size > 32 || batch < 1 || q_len < 1 || num_q_heads < 1 ||
       head_dim_v < 4)
@@ -276,15 +313,27 @@ DCP_API void dcp_testing_set_hooks(unsigned long long wait_ns, int32_t skip_tile
 }
 
 dcp_status_t dcp_get_last_device_status(void* stream) {
-  int* p = status_ptr();
-  if (!p) return DCP_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(s) != cudaSuccess) return DCP_ERR_CUDA;
+  int* p = status_ptr(s);
+  if (!p) return DCP_ERR_CUDA;
+  // read and clear the word on the stream itself: later work on the stream
+  // sees it cleared; no other stream is waited for
   int v = 0;
-  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DCP_ERR_CUDA;
-  if (cudaMemset(p, 0, sizeof(int)) != cudaSuccess) return DCP_ERR_CUDA;
-  if (cudaDeviceSynchronize() != cudaSuccess) return DCP_ERR_CUDA;
+  if (cudaMemcpyAsync(&v, p, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return DCP_ERR_CUDA;
+  if (cudaMemsetAsync(p, 0, sizeof(int), s) != cudaSuccess) return DCP_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DCP_ERR_CUDA;
   return static_cast<dcp_status_t>(v);
+}
+
+int32_t dcp_decode_attn_kernel_kind(const dcp_attn_desc_t* d, int32_t dcp_size) {
+  AttnArgs a{};
+  if (make_args(d, dcp_size, 1, 1.0f, d ? d->q_len : 1, &a) != DCP_OK) return DCP_KERNEL_NONE;
+  switch (select_impl(a)) {
+    case Impl::kMlaTc: return DCP_KERNEL_MLA_TC;
+    case Impl::kGqaTc: return DCP_KERNEL_GQA_TC;
+    case Impl::kSimt:
+    default: return DCP_KERNEL_SIMT;
+  }
 }
 
 }  // extern "C"

@@ -25,9 +25,17 @@
  *    dcp_get_last_device_status.
  *  - Arguments are checked on the host first; a bad argument returns an error
  *    code and launches nothing.  Errors found on the device (a sequence shorter
- *    than its query, a block id out of range, a bounded wait that expired) set a
- *    device status word read by dcp_get_last_device_status; the kernels then
- *    skip the offending work unit.
+ *    than its query, a block id out of range, a bounded wait that expired) set
+ *    the status word of the stream the call was enqueued on, read by
+ *    dcp_get_last_device_status(stream); the kernels then skip the offending
+ *    work unit (its partial output 0, its LSE -inf).  Each stream has its own
+ *    word, so concurrent streams do not see or clear each other's errors, up to
+ *    DCP_STATUS_STREAMS - 1 streams per device; further streams share one word.
+ *  - The first call of any entry point on a device looks up the status words'
+ *    device address; make it before any stream capture.  A captured call keeps
+ *    the status word of the stream it was captured on: errors of its replays
+ *    are read through that stream's handle.
+ *  - Every call is wrapped in an NVTX range named after it.
  *  - No C++ exception crosses this interface.
  *  - Integer tensors are int32, row-major (C order), without padding.
  */
@@ -57,6 +65,20 @@ typedef enum {
 } dcp_status_t;
 
 typedef enum { DCP_ATTN_GQA = 0, DCP_ATTN_MLA = 1 } dcp_attn_kind_t;
+
+/* Status words per device: one per stream, in order of first use. */
+#define DCP_STATUS_STREAMS 64
+
+/* The kernel dcp_decode_attn runs for a shape (dcp_decode_attn_kernel_kind). */
+typedef enum {
+  DCP_KERNEL_NONE = 0,     /* the shape is rejected                                   */
+  DCP_KERNEL_MLA_TC = 1,   /* tensor-core MLA kernel: Hq 128, Dqk 576, Dv 512, block 128 */
+  DCP_KERNEL_GQA_TC = 2,   /* tensor-core GQA kernel: head dim 64 or 128, block size a
+                              multiple of 8 that divides or is a multiple of 128       */
+  DCP_KERNEL_SIMT = 3      /* generic CUDA-core kernel for every other shape; an order of
+                              magnitude slower than the tensor-core kernels on the
+                              large shapes                                            */
+} dcp_kernel_kind_t;
 
 /* Shape of one decode-attention call.
  *  kind            DCP_ATTN_GQA or DCP_ATTN_MLA
@@ -215,8 +237,15 @@ DCP_API dcp_status_t dcp_kv_cache_write(const dcp_attn_desc_t* d, const void* ne
                                         int32_t dcp_size, int32_t interleave, int32_t n_new,
                                         void* stream);
 
-/* Synchronises `stream`, returns the device status word set by earlier kernels
- * (DCP_OK if none) and clears it. */
+/* Which kernel dcp_decode_attn would run for this shape (a dcp_kernel_kind_t;
+ * DCP_KERNEL_NONE for an invalid descriptor).  Host only, no GPU work: lets a
+ * caller see in advance that a shape falls back to the CUDA-core kernel. */
+DCP_API int32_t dcp_decode_attn_kernel_kind(const dcp_attn_desc_t* d, int32_t dcp_size);
+
+/* Reads `stream`'s status word (the first device-side error of the calls
+ * enqueued on that stream since the last read; DCP_OK if none) and clears it.
+ * The read and the clear are enqueued on `stream` and the call then waits for
+ * that stream only (no device-wide synchronisation). */
 DCP_API dcp_status_t dcp_get_last_device_status(void* stream);
 
 /* Static, human-readable name of a status code. */

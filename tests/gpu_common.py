@@ -27,7 +27,7 @@ def run_gpu(inst, dcp_size=None, interleave=None, stream=None):
                                   stream=stream)
     out, out_lse = dcp.dcp_merge(po, lse, N, stream=stream)
     torch.cuda.synchronize()
-    status = dcp.dcp_get_last_device_status()
+    status = dcp.dcp_get_last_device_status(stream)
     return {"partial_out": po.cpu().numpy(), "lse": lse.cpu().numpy(),
             "out": out.float().cpu().numpy(), "out_lse": out_lse.cpu().numpy(),
             "status": status}

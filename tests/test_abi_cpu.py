@@ -190,3 +190,22 @@ def test_split_planner_follows_the_wave_model(lib, kw, N, tile, units_per_split)
     want = 0 if n == 1 else ((rows * n * kw["head_dim_v"] * 4 + 255) & ~255) + rows * n * 4
     assert n > 1
     assert ws == want, (ws, want, n)
+
+
+@pytest.mark.parametrize("shape,N,want", [
+    (("mla", 4, 1, 128, 1, 576, 512, 128, 100, 10), 8, "MLA_TC"),
+    (("mla", 4, 4, 128, 1, 576, 512, 128, 100, 10), 8, "MLA_TC"),
+    (("mla", 4, 1, 64, 1, 576, 512, 128, 100, 10), 8, "SIMT"),      # fewer heads per rank
+    (("mla", 4, 1, 128, 1, 576, 512, 64, 100, 10), 8, "SIMT"),      # block size 64
+    (("gqa", 4, 1, 64, 4, 128, 128, 128, 100, 10), 4, "GQA_TC"),
+    (("gqa", 4, 1, 8, 2, 64, 64, 16, 100, 10), 2, "GQA_TC"),
+    (("gqa", 4, 1, 8, 2, 96, 96, 16, 100, 10), 2, "SIMT"),          # head dim 96
+    (("gqa", 4, 1, 8, 2, 64, 64, 48, 100, 10), 2, "SIMT"),          # block size 48
+    (("gqa", 4, 1, 8, 3, 64, 64, 16, 100, 10), 2, "NONE"),          # Hq % Hkv != 0
+    (("mla", 4, 1, 128, 2, 576, 512, 128, 100, 10), 8, "NONE"),     # MLA with 2 KV heads
+])
+def test_kernel_kind_reports_the_kernel_a_shape_runs(lib, shape, N, want):
+    """The host-side query names the kernel dcp_decode_attn selects, so a caller
+    sees a fall-back to the CUDA-core kernel before launching."""
+    desc = lib.make_desc(*shape)
+    assert lib.dcp_decode_attn_kernel_kind(desc, N) == getattr(lib, "DCP_KERNEL_" + want)

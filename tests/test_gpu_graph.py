@@ -67,7 +67,7 @@ def test_decode_step_replays_from_a_cuda_graph(name, kw):
     torch.cuda.current_stream().wait_stream(s)
     g.replay()
     torch.cuda.synchronize()
-    assert dcp.dcp_get_last_device_status() == dcp.DCP_OK
+    assert dcp.dcp_get_last_device_status(s) == dcp.DCP_OK      # the captured calls' status word
     for a, b in zip((po, lse, out, out_lse), eager):
         assert torch.equal(a, b)
 
