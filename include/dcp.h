@@ -153,7 +153,24 @@ DCP_API size_t dcp_decode_attn_workspace_size(const dcp_attn_desc_t* d, int32_t 
  * Alignment: q, kv_cache, partial_out 16 bytes.
  * Errors: INVALID_ARG (NULL pointers, sizes < 1, Hq % Hkv != 0, MLA with
  * Hkv != 1 or Dv > Dqk, GQA with Dv != Dqk, causal_q_len != q_len, small
- * workspace, misalignment); UNSUPPORTED (head dims without a kernel); CUDA.  */
+ * workspace, misalignment); UNSUPPORTED (head dims without a kernel); CUDA.
+ * Arithmetic and accuracy: products of the bf16 inputs accumulate in fp32;
+ * the softmax runs in fp32 in the log2 domain.  Each probability is rounded to
+ * bf16 once before the value product (the GQA tensor-core kernel carries it as
+ * two bf16 terms, hi + lo, so about 16 bits reach the product).  Against the
+ * fp64 definition above, partial_out is within 2e-3 absolute + 1e-2 relative
+ * and lse within 1e-3 absolute; the tests hold that bar for softmaxes
+ * dominated by one or a few keys and for scaled scores of 30-60 (sinks).
+ * The MLA tensor-core kernel forms every score from two halves computed on
+ * the two CTAs of a cluster pair; a half crosses the pair as a 16-bit code
+ * with one power-of-two scale per head and 64-key tile (absolute error at most
+ * 2^-14 * the head's largest |half| in that tile).  When some head's largest
+ * |half| * scale * log2(e) exceeds 8, the 16-bit residual of every code is
+ * sent as well, and the error drops to at most 2^-29 * that largest |half|,
+ * below fp32 rounding of the score itself.  Magnitude limit: halves up to
+ * 2^74 in magnitude (|q . k| about 1.9e22) are encoded; past that the
+ * received score is undefined.  A half sums 288 products, so queries and
+ * keys with every |q_d|, |k_d| <= 2^31 stay inside the limit.  */
 DCP_API dcp_status_t dcp_decode_attn(const dcp_attn_desc_t* d, const void* q, const void* kv_cache,
                              const int32_t* block_tables, const int32_t* seq_lens,
                              int32_t dcp_size, int32_t interleave, float scale,
