@@ -76,16 +76,20 @@ def algorithmic(w: wl.Workload, seq_lens) -> dict:
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one attention
 # launch, as a multiple of its algorithmic bytes, from an ncu capture of a
 # smaller case of the same kernel (traffic scales with the cache bytes
-# processed).  Keyed by the kernel source the counters were taken on: once the
-# source changes, traffic is reported as null.
+# processed): MLA from the batch-32 workload, GQA from the Qwen-like one, and
+# the 64-token chunk workload from its own capture (its 64 queries per shard
+# share the key stream through L2, so its ratio differs).  Keyed by the kernel
+# source the counters were taken on: once the source changes, traffic is
+# reported as null.
 NCU_TRAFFIC_RATIO = {
-    "mla": ("72df035987125067", 1.00760, "attn_mla_tc.cu"),
-    "gqa": ("de022da015e73ab4", 1.00383, "attn_gqa_tc.cu"),
+    "mla": ("0da2eabba4c7f5a1", 1.00628, "attn_mla_tc.cu"),
+    "gqa": ("f6e04d4ccaedbfff", 1.00386, "attn_gqa_tc.cu"),
+    "mla_chunk64": ("0da2eabba4c7f5a1", 1.04527, "attn_mla_tc.cu"),
 }
 
 
-def measured_traffic(kind: str, alg_bytes: int):
-    sha, ratio, fname = NCU_TRAFFIC_RATIO[kind]
+def measured_traffic(w: wl.Workload, alg_bytes: int):
+    sha, ratio, fname = NCU_TRAFFIC_RATIO.get(w.name, NCU_TRAFFIC_RATIO[w.kind])
     path = os.path.join(ROOT, "context_decode_attention_paged_gb300", "csrc", fname)
     with open(path, "rb") as f:
         cur = hashlib.sha256(f.read()).hexdigest()[:16]
@@ -330,7 +334,7 @@ def cpu_threads() -> int:
 
 # The other workload configurations, measured in the same run after the headline
 # one and reported beside it (single GPU).
-OTHER_CONFIGS = ("tiny_gqa", "qwen_gqa", "mla_32", "mla_mtp")
+OTHER_CONFIGS = ("tiny_gqa", "qwen_gqa", "mla_32", "mla_mtp", "mla_chunk64")
 
 
 def roofline_of(w, alg, attn_ms: float, peaks) -> dict:
@@ -556,7 +560,7 @@ def run_ours(args):
     else:
         roof = {"bound": "tensor", "achieved": round(attn_tfs, 1), "peak": tflops,
                 "unit": "TFLOP/s", "frac": round(attn_tfs / tflops, 4)}
-    roof.update({"traffic": measured_traffic(w.kind, alg["attn_bytes"]), "peak_source": f"{peak_src} (MEASURED_PEAKS.json)"
+    roof.update({"traffic": measured_traffic(w, alg["attn_bytes"]), "peak_source": f"{peak_src} (MEASURED_PEAKS.json)"
                  if peak_src == "measured" else "fallback",
                  "kernel": "dcp_decode_attn", "attn_ms": round(attn_avg, 4),
                  "attn_ms_median": round(statistics.median(attn_ms), 4),

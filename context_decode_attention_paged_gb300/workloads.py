@@ -73,6 +73,13 @@ WORKLOADS = {
         head_dim_qk=576, head_dim_v=512, block_size=128, dcp_size=8, interleave=128,
         scale=1.0 / math.sqrt(192.0), std=0.5,
         lengths=("lognormal", 67000, 0.25, 4096, 200000), permute_blocks=True, seed=1004),
+    # chunked prefill under DCP: 64 causal query tokens per request attend to
+    # the sharded cache; the 64 queries of a shard read the same keys
+    "mla_chunk64": Workload(
+        "mla_chunk64", "mla", batch=4, q_len=64, num_q_heads=128, num_kv_heads=1,
+        head_dim_qk=576, head_dim_v=512, block_size=128, dcp_size=8, interleave=128,
+        scale=1.0 / math.sqrt(192.0), std=0.5,
+        lengths=("lognormal", 67000, 0.25, 4096, 200000), permute_blocks=True, seed=1006),
     # length stress variant of mla_512: log-normal sigma 1.0 (same median and
     # clip), ~51 GB of cache; reported beside the main workload
     "mla_512_s1": Workload(

@@ -25,7 +25,11 @@ from oracle import dcp_oracle as orc
 
 pytestmark = pytest.mark.gpu
 
-FULL = ["qwen_gqa", "mla_32", "mla_mtp", "mla_512", "mla_512_s1"]
+FULL = ["qwen_gqa", "mla_32", "mla_mtp", "mla_512", "mla_512_s1", "mla_chunk64"]
+# long query chunks: these query rows of every request are checked; query i
+# at position S - Lq + i sees what a one-token decode of context S - Lq + i + 1
+# sees, which keeps the oracle's work to a few decodes per request
+CHUNK_ROWS = (0, 1, 31, 62, 63)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -72,6 +76,9 @@ def test_full_size_against_oracle(name):
 
         # requests element by element, a few at a time (bounded host memory)
         idx_all = _checked_requests(w)
+        if w.q_len > 4:
+            _check_chunk_rows(w, inst, po, lse, out, out_lse, idx_all)
+            return
         for c0 in range(0, len(idx_all), 8):
             idx = idx_all[c0:c0 + 8]
             q, kv, bt, sl = bench.host_sample(inst, idx)
@@ -86,3 +93,19 @@ def test_full_size_against_oracle(name):
     finally:
         del inst
         torch.cuda.empty_cache()
+
+
+def _check_chunk_rows(w, inst, po, lse, out, out_lse, idx_all):
+    """Sampled query rows of a long causal chunk, each against the oracle's
+    one-token decode of the context that row sees."""
+    for b in idx_all:
+        q, kv, bt, sl = bench.host_sample(inst, [b])
+        for i in CHUNK_ROWS:
+            s_i = np.array([int(sl[0]) - w.q_len + i + 1], dtype=sl.dtype)
+            ref = orc.ref_dcp_decode(w.kind, orc.to_f64(q[:, i:i + 1]), orc.to_f64(kv), bt, s_i, w.dcp_size,
+                                     w.interleave, w.block_size, w.scale, 1, w.head_dim_v)
+            tag = f"{w.name} request {b} query {i}"
+            assert_close(out[:, b:b + 1, i:i + 1].float().cpu().numpy(), ref["out"], f"{tag} out")
+            assert_lse_close(out_lse[:, b:b + 1, i:i + 1].cpu().numpy(), ref["out_lse"], f"{tag} out_lse")
+            assert_close(po[:, b:b + 1, i:i + 1].cpu().numpy(), ref["partial_out"], f"{tag} partial_out")
+            assert_lse_close(lse[:, b:b + 1, i:i + 1].cpu().numpy(), ref["lse"], f"{tag} lse")
