@@ -67,7 +67,7 @@ using namespace sm100;
 
 constexpr int kHeads = 128;
 constexpr int kDqk = 576, kDv = 512, kLatent = 512;
-constexpr int kNt = 64;                        // tokens per KV tile (half a 128-token block)
+constexpr int kNt = 64;                        // tokens per KV tile
 constexpr int kHalf = 32;                      // tokens of a tile whose softmax a CTA owns
 constexpr int kStages = 5;
 constexpr uint32_t kChunkBytes = kNt * 128;    // 64 tokens x 64 dims bf16, 128B rows
@@ -718,7 +718,7 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
     // DCP_ERR_BOUNDS; both CTAs of the pair read the same entries
     const int32_t* bt = p.block_tables + ((long long)u.r * p.B + u.b) * p.max_lb;
     bool bad_blk = false;
-    for (int jb = tid; jb < (vis + 127) / 128; jb += (int)kThreads)   // every split of the query
+    for (int jb = tid; jb < (vis + p.bs - 1) / p.bs; jb += (int)kThreads)   // every split of the query
       bad_blk |= (unsigned)bt[jb] >= (unsigned)p.num_blocks;
     if (__syncthreads_or(bad_blk)) {
       u.T = 0;
@@ -736,20 +736,27 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
   int issued[kStages];
 #pragma unroll
   for (int k = 0; k < kStages; ++k) issued[k] = 0;
+  const int box_rows = p.bs < kNt ? p.bs : kNt;
+  const int boxes = kNt / box_rows;
   auto issue_tile = [&](int t) {
     // test hook: CTA 0 never loads this tile, so the bounded waits on it run
     // out and the unit unwinds
     if (t == p.skip_tile && cta == 0) return;
-    const int j = u.kb + t * kNt;
-    const int row = bt_row[j / 128] * 128 + (j & 127);   // block ids were checked against the pool above
     const int st = t % kStages;
     const uint32_t full = smem_u32(&sm.kv_full[st]);
     uint8_t* dst = stages + st * kStageBytes;
     mbar_arrive_expect_tx(full, kStageBytes);
+    // a tile is one box of 64 rows (blocks of 64 tokens or a multiple) or one
+    // box per block (blocks of 8, 16 or 32); boxes past the key range read pool
+    // row 0 (masked, values zeroed) so that no stale table entry is followed
+    for (int k = 0; k < boxes; ++k) {
+      const int j = u.kb + t * kNt + k * box_rows;
+      const int row = j < u.ke ? bt_row[j / p.bs] * p.bs + (j % p.bs) : 0;   // ids checked against the pool above
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      tma_load_2d(smem_u32(dst + c * kChunkBytes), &tm_lat, 256 * (int)cta + 64 * c, row, full);
-    tma_load_2d(smem_u32(dst + 4 * kChunkBytes), &tm_rope, kLatent + 32 * (int)cta, row, full);
+      for (int c = 0; c < 4; ++c)
+        tma_load_2d(smem_u32(dst + c * kChunkBytes + k * box_rows * 128), &tm_lat, 256 * (int)cta + 64 * c, row, full);
+      tma_load_2d(smem_u32(dst + 4 * kChunkBytes + k * box_rows * 64), &tm_rope, kLatent + 32 * (int)cta, row, full);
+    }
     ++issued[st];
   };
   // the query slice by TMA: latent dims 0-63 and the rope dims straight into
@@ -928,7 +935,8 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
 
 bool mla_tc_supported(const AttnArgs& a) {
   return a.kind == DCP_ATTN_MLA && a.Hq == kHeads && a.Hkv == 1 && a.Dqk == kDqk && a.Dv == kDv &&
-         a.bs == 128 && (long long)a.num_blocks * a.bs < (1LL << 31);
+         (a.bs == 8 || a.bs == 16 || a.bs == 32 || a.bs % kNt == 0) &&
+         (long long)a.num_blocks * a.bs < (1LL << 31);
 }
 
 SplitPlan plan_attn_mla_tc(const AttnArgs& a, int sm_count) {
@@ -939,8 +947,9 @@ cudaError_t launch_attn_mla_tc(const AttnArgs& a, const SplitPlan& plan) {
   CUtensorMap tm_lat, tm_rope;
   const uint64_t dims[2] = {(uint64_t)kDqk, (uint64_t)a.num_blocks * a.bs};
   const uint64_t strides[1] = {(uint64_t)kDqk * 2};
-  const uint32_t box_lat[2] = {64, kNt};
-  const uint32_t box_rope[2] = {32, kNt};
+  const uint32_t box_rows = (uint32_t)(a.bs < kNt ? a.bs : kNt);
+  const uint32_t box_lat[2] = {64, box_rows};
+  const uint32_t box_rope[2] = {32, box_rows};
   if (!make_tensor_map_bf16(&tm_lat, a.kv, 2, dims, strides, box_lat, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tensor_map_bf16(&tm_rope, a.kv, 2, dims, strides, box_rope, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;

@@ -196,7 +196,9 @@ def test_split_planner_follows_the_wave_model(lib, kw, N, tile, units_per_split)
     (("mla", 4, 1, 128, 1, 576, 512, 128, 100, 10), 8, "MLA_TC"),
     (("mla", 4, 4, 128, 1, 576, 512, 128, 100, 10), 8, "MLA_TC"),
     (("mla", 4, 1, 64, 1, 576, 512, 128, 100, 10), 8, "SIMT"),      # fewer heads per rank
-    (("mla", 4, 1, 128, 1, 576, 512, 64, 100, 10), 8, "SIMT"),      # block size 64
+    (("mla", 4, 1, 128, 1, 576, 512, 64, 100, 10), 8, "MLA_TC"),    # block size 64
+    (("mla", 4, 1, 128, 1, 576, 512, 16, 100, 10), 8, "MLA_TC"),    # block size 16 (four boxes a tile)
+    (("mla", 4, 1, 128, 1, 576, 512, 48, 100, 10), 8, "SIMT"),      # block size 48
     (("gqa", 4, 1, 64, 4, 128, 128, 128, 100, 10), 4, "GQA_TC"),
     (("gqa", 4, 1, 8, 2, 64, 64, 16, 100, 10), 2, "GQA_TC"),
     (("gqa", 4, 1, 8, 2, 96, 96, 16, 100, 10), 2, "SIMT"),          # head dim 96

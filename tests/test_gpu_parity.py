@@ -104,6 +104,17 @@ ATTN_CASES = [
     ("qwen_gqa", dict(batch=2, block_size=64, lengths=("uniform", 700, 2000), dcp_size=2, interleave=64)),
     ("qwen_gqa", dict(batch=2, block_size=256, lengths=("uniform", 700, 3000), dcp_size=2, interleave=256)),
     ("tiny_gqa", dict(block_size=48, lengths=("fixed", 700), dcp_size=2, interleave=48)),
+    # MLA block sizes: one TMA box per block in a 64-key tile (8, 16, 32), one
+    # block per tile (64), a block spanning four tiles (256), with ragged tails
+    # and a KV split; 48 is declined by the tensor-core kernel
+    ("mla_32", dict(batch=2, block_size=8, lengths=("uniform", 300, 1300), dcp_size=2, interleave=8)),
+    ("mla_32", dict(batch=2, block_size=16, lengths=("uniform", 300, 1300), dcp_size=4, interleave=1)),
+    ("mla_32", dict(batch=3, block_size=32, q_len=2, lengths=("uniform", 200, 2000), dcp_size=2,
+                    interleave=32)),
+    ("mla_32", dict(batch=2, block_size=64, lengths=("uniform", 700, 3000), dcp_size=2, interleave=64)),
+    ("mla_32", dict(batch=1, block_size=64, lengths=("fixed", 9000), dcp_size=1)),
+    ("mla_32", dict(batch=2, block_size=256, lengths=("uniform", 700, 3000), dcp_size=2, interleave=256)),
+    ("mla_32", dict(batch=2, block_size=48, lengths=("uniform", 100, 700), dcp_size=2, interleave=48)),
     # group sizes: 1 (one real row of a 16-row tile) and 8 with Lq 3 (24 rows of a 32-row tile)
     ("qwen_gqa", dict(batch=2, num_q_heads=8, num_kv_heads=8, lengths=("uniform", 300, 900), dcp_size=2)),
     ("qwen_gqa", dict(batch=2, num_q_heads=32, num_kv_heads=4, q_len=3, lengths=("uniform", 300, 900),

@@ -73,6 +73,8 @@ POISON_CASES = [
     ("tiny_gqa", dict(batch=4, dcp_size=2, interleave=16)),                    # bs 16, D 64
     ("mla_32", dict(batch=4, dcp_size=1, interleave=128)),                     # tensor-core MLA
     ("mla_32", dict(batch=4, dcp_size=4, interleave=1, q_len=4)),
+    ("mla_32", dict(batch=4, dcp_size=2, interleave=16, block_size=16)),      # four boxes per tile
+    ("mla_32", dict(batch=4, dcp_size=1, interleave=64, block_size=64)),
     ("tiny_gqa", dict(batch=4, dcp_size=2, interleave=16, head_dim_qk=96, head_dim_v=96)),   # SIMT
     ("mla_32", dict(batch=4, dcp_size=2, interleave=128, num_q_heads=16, head_dim_qk=72,
                     head_dim_v=64)),                                           # SIMT, MLA layout
