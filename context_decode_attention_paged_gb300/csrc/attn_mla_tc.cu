@@ -117,7 +117,7 @@ struct MlaParams {
   float* dst_o;        // partial_out, or the split workspace
   float* dst_lse;
   int* status;
-  int B, Lq, N, I, max_lb, bs, num_blocks, n_split, split_tokens;
+  int B, Lq, Hq, N, I, max_lb, bs, num_blocks, n_split, split_tokens;
   float scale_log2;    // scale * log2(e)
   unsigned long long wait_ns;   // limit of every bounded wait
   int skip_tile;                // test hook: CTA 0 never loads this tile (-1: off)
@@ -505,17 +505,20 @@ __device__ __forceinline__ void softmax_wg(const MlaParams& p, Smem& sm, const U
   named_bar_sync(kBarEpi, 256);
   // ... and out to HBM as whole 1 KB row segments: warp k of the 8 writes the
   // rows of heads [16k, 16k + 16), 512 contiguous bytes per store instruction
-  const long long row0 = ((((long long)u.r * p.B + u.b) * p.Lq + u.i_q) * p.n_split + u.s_idx) * kHeads;
+  // (with fewer than 128 query heads the MMA rows past Hq hold the next query
+  // rows of the tensor: computed, never written)
+  const long long row0 = ((((long long)u.r * p.B + u.b) * p.Lq + u.i_q) * p.n_split + u.s_idx) * p.Hq;
   const int wi = 4 * w + lg;
   for (int rr = 0; rr < 16; ++rr) {
     const int hr = 16 * wi + rr;
+    if (hr >= p.Hq) break;
     float4* g = reinterpret_cast<float4*>(p.dst_o + (row0 + hr) * kDv + 256 * cta);
     const float4* sp = reinterpret_cast<const float4*>(ostage + hr * kOPitch);
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     g[lane] = have ? sp[lane] : z;
     g[32 + lane] = have ? sp[32 + lane] : z;
   }
-  if (cta == 0 && w == 0)
+  if (cta == 0 && w == 0 && h < p.Hq)
     p.dst_lse[row0 + h] = (have && l_tot > 0.f) ? (r_fin + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
 }
 
@@ -616,7 +619,7 @@ __device__ __forceinline__ void score_sender(const MlaParams& p, Smem& sm, const
   }
 }
 
-template <bool kLpt>
+template <bool kLpt, bool kSmallBlocks>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
                 const __grid_constant__ CUtensorMap tm_qlat, const __grid_constant__ CUtensorMap tm_qrope,
@@ -736,8 +739,6 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
   int issued[kStages];
 #pragma unroll
   for (int k = 0; k < kStages; ++k) issued[k] = 0;
-  const int box_rows = p.bs < kNt ? p.bs : kNt;
-  const int boxes = kNt / box_rows;
   auto issue_tile = [&](int t) {
     // test hook: CTA 0 never loads this tile, so the bounded waits on it run
     // out and the unit unwinds
@@ -746,16 +747,26 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
     const uint32_t full = smem_u32(&sm.kv_full[st]);
     uint8_t* dst = stages + st * kStageBytes;
     mbar_arrive_expect_tx(full, kStageBytes);
-    // a tile is one box of 64 rows (blocks of 64 tokens or a multiple) or one
-    // box per block (blocks of 8, 16 or 32); boxes past the key range read pool
-    // row 0 (masked, values zeroed) so that no stale table entry is followed
-    for (int k = 0; k < boxes; ++k) {
-      const int j = u.kb + t * kNt + k * box_rows;
-      const int row = j < u.ke ? bt_row[j / p.bs] * p.bs + (j % p.bs) : 0;   // ids checked against the pool above
+    if (!kSmallBlocks) {
+      // blocks of 64 tokens or a multiple: the tile is one box inside one block
+      const int j = u.kb + t * kNt;
+      const int row = bt_row[j / p.bs] * p.bs + (j % p.bs);   // ids checked against the pool above
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        tma_load_2d(smem_u32(dst + c * kChunkBytes + k * box_rows * 128), &tm_lat, 256 * (int)cta + 64 * c, row, full);
-      tma_load_2d(smem_u32(dst + 4 * kChunkBytes + k * box_rows * 64), &tm_rope, kLatent + 32 * (int)cta, row, full);
+        tma_load_2d(smem_u32(dst + c * kChunkBytes), &tm_lat, 256 * (int)cta + 64 * c, row, full);
+      tma_load_2d(smem_u32(dst + 4 * kChunkBytes), &tm_rope, kLatent + 32 * (int)cta, row, full);
+    } else {
+      // blocks of 8, 16 or 32 tokens: one box per block; boxes past the key
+      // range read pool row 0 (masked, values zeroed) so that no stale table
+      // entry is followed
+      for (int k = 0; k < kNt / p.bs; ++k) {
+        const int j = u.kb + t * kNt + k * p.bs;
+        const int row = j < u.ke ? bt_row[j / p.bs] * p.bs : 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tma_load_2d(smem_u32(dst + c * kChunkBytes + k * p.bs * 128), &tm_lat, 256 * (int)cta + 64 * c, row, full);
+        tma_load_2d(smem_u32(dst + 4 * kChunkBytes + k * p.bs * 64), &tm_rope, kLatent + 32 * (int)cta, row, full);
+      }
     }
     ++issued[st];
   };
@@ -767,7 +778,7 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
   if (warp == 0 && lane == 0 && T > 0) {
     prefetch_tmap(&tm_lat);
     prefetch_tmap(&tm_rope);
-    const int32_t qr = (int32_t)(((long long)u.b * p.Lq + u.i_q) * kHeads);
+    const int32_t qr = (int32_t)(((long long)u.b * p.Lq + u.i_q) * p.Hq);
     const uint32_t qf = smem_u32(&sm.q_full);
     mbar_arrive_expect_tx(qf, kQLat0Bytes * 4 + kQRopeBytes);
     tma_load_2d(smem_u32(qlat0), &tm_qlat, 256 * (int)cta, qr, qf);
@@ -934,7 +945,10 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
 }  // namespace
 
 bool mla_tc_supported(const AttnArgs& a) {
-  return a.kind == DCP_ATTN_MLA && a.Hq == kHeads && a.Hkv == 1 && a.Dqk == kDqk && a.Dv == kDv &&
+  // 16 to 128 query heads; the query box is 128 rows, so the query tensor
+  // must hold at least that many
+  return a.kind == DCP_ATTN_MLA && a.Hq >= 16 && a.Hq <= kHeads && (long long)a.B * a.Lq * a.Hq >= kHeads &&
+         a.Hkv == 1 && a.Dqk == kDqk && a.Dv == kDv &&
          (a.bs == 8 || a.bs == 16 || a.bs == 32 || a.bs % kNt == 0) &&
          (long long)a.num_blocks * a.bs < (1LL << 31);
 }
@@ -968,6 +982,7 @@ cudaError_t launch_attn_mla_tc(const AttnArgs& a, const SplitPlan& plan) {
   p.status = a.status;
   p.B = a.B;
   p.Lq = a.Lq;
+  p.Hq = a.Hq;
   p.N = a.N;
   p.I = a.I;
   p.max_lb = a.max_lb;
@@ -987,9 +1002,10 @@ cudaError_t launch_attn_mla_tc(const AttnArgs& a, const SplitPlan& plan) {
     p.dst_o = a.partial_out;
     p.dst_lse = a.lse;
   }
-  const bool lpt = a.B <= kLptMaxBatch;
+  const bool lpt = a.B <= kLptMaxBatch, small = a.bs < kNt;
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const MlaParams) =
-      lpt ? mla_attn_kernel<true> : mla_attn_kernel<false>;
+      lpt ? (small ? mla_attn_kernel<true, true> : mla_attn_kernel<true, false>)
+          : (small ? mla_attn_kernel<false, true> : mla_attn_kernel<false, false>);
   // the register split assumes the compiled launch count; refuse to launch
   // otherwise (setmaxnreg.inc would wait for registers that do not exist)
   cudaFuncAttributes fa;

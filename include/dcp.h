@@ -72,8 +72,8 @@ typedef enum { DCP_ATTN_GQA = 0, DCP_ATTN_MLA = 1 } dcp_attn_kind_t;
 /* The kernel dcp_decode_attn runs for a shape (dcp_decode_attn_kernel_kind). */
 typedef enum {
   DCP_KERNEL_NONE = 0,     /* the shape is rejected                                   */
-  DCP_KERNEL_MLA_TC = 1,   /* tensor-core MLA kernel: Hq 128, Dqk 576, Dv 512, block size
-                              8, 16, 32 or a multiple of 64                            */
+  DCP_KERNEL_MLA_TC = 1,   /* tensor-core MLA kernel: Hq 16-128 (B * Lq * Hq >= 128),
+                              Dqk 576, Dv 512, block size 8, 16, 32 or a multiple of 64 */
   DCP_KERNEL_GQA_TC = 2,   /* tensor-core GQA kernel: head dim 64 or 128, block size a
                               multiple of 8 that divides or is a multiple of 128       */
   DCP_KERNEL_SIMT = 3      /* generic CUDA-core kernel for every other shape; an order of

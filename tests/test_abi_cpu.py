@@ -195,7 +195,9 @@ def test_split_planner_follows_the_wave_model(lib, kw, N, tile, units_per_split)
 @pytest.mark.parametrize("shape,N,want", [
     (("mla", 4, 1, 128, 1, 576, 512, 128, 100, 10), 8, "MLA_TC"),
     (("mla", 4, 4, 128, 1, 576, 512, 128, 100, 10), 8, "MLA_TC"),
-    (("mla", 4, 1, 64, 1, 576, 512, 128, 100, 10), 8, "SIMT"),      # fewer heads per rank
+    (("mla", 4, 1, 64, 1, 576, 512, 128, 100, 10), 8, "MLA_TC"),    # 64 heads: MMA rows past 64 unused
+    (("mla", 1, 1, 64, 1, 576, 512, 128, 100, 10), 8, "SIMT"),      # a query tensor under 128 rows
+    (("mla", 4, 1, 8, 1, 576, 512, 128, 100, 10), 8, "SIMT"),       # under 16 heads
     (("mla", 4, 1, 128, 1, 576, 512, 64, 100, 10), 8, "MLA_TC"),    # block size 64
     (("mla", 4, 1, 128, 1, 576, 512, 16, 100, 10), 8, "MLA_TC"),    # block size 16 (four boxes a tile)
     (("mla", 4, 1, 128, 1, 576, 512, 48, 100, 10), 8, "SIMT"),      # block size 48

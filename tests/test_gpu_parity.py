@@ -115,6 +115,12 @@ ATTN_CASES = [
     ("mla_32", dict(batch=1, block_size=64, lengths=("fixed", 9000), dcp_size=1)),
     ("mla_32", dict(batch=2, block_size=256, lengths=("uniform", 700, 3000), dcp_size=2, interleave=256)),
     ("mla_32", dict(batch=2, block_size=48, lengths=("uniform", 100, 700), dcp_size=2, interleave=48)),
+    # MLA with fewer query heads per rank (the MMA rows past Hq hold other
+    # queries' rows, computed and discarded), odd counts included
+    ("mla_32", dict(batch=3, num_q_heads=64, lengths=("uniform", 300, 2000), dcp_size=4)),
+    ("mla_32", dict(batch=2, num_q_heads=16, q_len=4, lengths=("uniform", 300, 1500), dcp_size=2,
+                    interleave=1)),
+    ("mla_32", dict(batch=3, num_q_heads=40, lengths=("uniform", 700, 3000), dcp_size=8)),
     # group sizes: 1 (one real row of a 16-row tile) and 8 with Lq 3 (24 rows of a 32-row tile)
     ("qwen_gqa", dict(batch=2, num_q_heads=8, num_kv_heads=8, lengths=("uniform", 300, 900), dcp_size=2)),
     ("qwen_gqa", dict(batch=2, num_q_heads=32, num_kv_heads=4, q_len=3, lengths=("uniform", 300, 900),
