@@ -662,12 +662,13 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
   }
   Unit u;
   {
-    const long long per_req = (long long)p.N * p.Lq * p.n_split;
-    const long long rest = kLpt ? unit % per_req : unit;
-    u.s_idx = (int)(rest % p.n_split);
-    u.i_q = (int)((rest / p.n_split) % p.Lq);
-    u.b = kLpt ? b_lpt : (int)((unit / ((long long)p.n_split * p.Lq)) % p.B);
-    u.r = kLpt ? (int)(rest / ((long long)p.n_split * p.Lq)) : (int)(unit / ((long long)p.n_split * p.Lq * p.B));
+    // 32-bit index arithmetic (the launcher keeps units below 2^31)
+    const unsigned un = (unsigned)unit, per_q = (unsigned)(p.n_split * p.Lq);
+    const unsigned rest = kLpt ? un % ((unsigned)p.N * per_q) : un;
+    u.s_idx = (int)(rest % (unsigned)p.n_split);
+    u.i_q = (int)((rest / (unsigned)p.n_split) % (unsigned)p.Lq);
+    u.b = kLpt ? b_lpt : (int)((un / per_q) % (unsigned)p.B);
+    u.r = kLpt ? (int)(rest / per_q) : (int)(un / (per_q * (unsigned)p.B));
   }
   // barriers and tensor memory first: they depend on no loaded data
   if (tid == 0) {
@@ -1016,6 +1017,7 @@ cudaError_t launch_attn_mla_tc(const AttnArgs& a, const SplitPlan& plan) {
   if (e != cudaSuccess) return e;
   const long long units = (long long)a.N * a.B * a.Lq * plan.n_split;
   if (units == 0) return cudaSuccess;
+  if (units > (1LL << 30)) return cudaErrorInvalidValue;   // two CTAs a unit; 32-bit unit indices
   kern<<<(unsigned)(2 * units), kThreads, kSmemBytes, a.stream>>>(tm_lat, tm_rope, tm_qlat, tm_qrope, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || plan.n_split <= 1) return e;
