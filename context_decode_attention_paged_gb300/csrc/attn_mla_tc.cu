@@ -107,7 +107,7 @@ constexpr uint32_t kColO = 256;    // 256 cols fp32 output
 constexpr float kLazyLog2 = 8.0f;       // R moves when scores pass it by more than this
 constexpr float kResidualLog2 = 8.0f;   // |partial| * scale above this (log2 units): send a residual
 constexpr uint32_t kBarEpi = 1;         // named barrier of the two softmax warpgroups (epilogue)
-constexpr int kOPitch = 260;            // floats per staged output row (1 KB + 16 B)
+constexpr uint32_t kOBoxBytes = kHeads * 128;   // staged output box: 128 rows x 32 fp32
 constexpr int kPvGate = 1;              // PV(t) waits for the score MMAs of tile t + kPvGate
 
 struct MlaParams {
@@ -153,7 +153,7 @@ struct Smem {
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kQRopeBytes + kQLat0Bytes + kScMsgBytes +
                               kPmMsgBytes + 2 * kMxMsgBytes + sizeof(Smem) + 64;
 static_assert(kSmemBytes <= 232448, "shared memory of the MLA kernel");
-static_assert(kHeads * kOPitch * 4 <= kStages * kStageBytes, "the staged output fits the ring");
+static_assert(8 * kOBoxBytes <= kStages * kStageBytes, "the staged output fits the ring");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -235,7 +235,8 @@ __device__ __forceinline__ int valid_of_half(const Unit& u, int t, int half) {
 // ---------------------------------------------------------------------------
 // softmax warpgroup w (tiles w, w + 2, ...)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void softmax_wg(const MlaParams& p, Smem& sm, const Unit& u, uint8_t* stages,
+__device__ __forceinline__ void softmax_wg(const MlaParams& p, const CUtensorMap& tm_out, Smem& sm, const Unit& u,
+                                           uint8_t* stages,
                                            const uint8_t* scbuf, const uint8_t* pmbuf, const float* mxbuf,
                                            uint32_t tmem, uint32_t cta, int warp, int lane) {
   const uint32_t peer = cta ^ 1u;
@@ -486,37 +487,47 @@ __device__ __forceinline__ void softmax_wg(const MlaParams& p, Smem& sm, const U
     l_tot = sm.lw[0][h] * ex2(sm.rlast[0][h] - r_fin) + sm.lw[1][h] * ex2(sm.rlast[1][h] - r_fin);
   }
   const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-  // this CTA's 256 output dims of head h, scaled by 1 / l, into shared memory
-  // (the ring is idle once every PV has landed; rows padded so that the
-  // stores of a warp's 32 heads spread over the banks) ...
-  float* ostage = reinterpret_cast<float*>(stages);
+  const long long row0 = ((((long long)u.r * p.B + u.b) * p.Lq + u.i_q) * p.n_split + u.s_idx) * p.Hq;
   if (have) {
+    // this CTA's 256 output dims of head h, scaled by 1 / l, into shared
+    // memory as eight boxes of 32 dims x 128 rows under the 128-byte swizzle
+    // (the ring is idle once every PV has landed; the swizzle spreads a
+    // warp's 32 rows over the banks) ...
+    uint8_t* ostage = stages;
+#pragma unroll 1
     for (int c = 0; c < 128; c += 32) {
       uint32_t v[32];
       tmem_ld32(lane_addr + kColO + 128 * w + c, v);
       tmem_wait_ld();
-      float4* dst = reinterpret_cast<float4*>(ostage + h * kOPitch + 128 * w + c);
+      uint8_t* row = ostage + (4 * w + c / 32) * kOBoxBytes + h * 128;
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        dst[k] = make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
-                             __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
+        *reinterpret_cast<float4*>(row + ((k ^ (h & 7)) << 4)) =
+            make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
+                        __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
     }
-  }
-  named_bar_sync(kBarEpi, 256);
-  // ... and out to HBM as whole 1 KB row segments: warp k of the 8 writes the
-  // rows of heads [16k, 16k + 16), 512 contiguous bytes per store instruction
-  // (with fewer than 128 query heads the MMA rows past Hq hold the next query
-  // rows of the tensor: computed, never written)
-  const long long row0 = ((((long long)u.r * p.B + u.b) * p.Lq + u.i_q) * p.n_split + u.s_idx) * p.Hq;
-  const int wi = 4 * w + lg;
-  for (int rr = 0; rr < 16; ++rr) {
-    const int hr = 16 * wi + rr;
-    if (hr >= p.Hq) break;
-    float4* g = reinterpret_cast<float4*>(p.dst_o + (row0 + hr) * kDv + 256 * cta);
-    const float4* sp = reinterpret_cast<const float4*>(ostage + hr * kOPitch);
+    fence_proxy_async_smem();
+    named_bar_sync(kBarEpi, 256);
+    // ... and out to HBM by TMA: one thread stores the boxes (Hq rows each:
+    // with fewer than 128 query heads the MMA rows past Hq hold the next query
+    // rows of the tensor, computed and never written) and waits only until
+    // they have been read out of shared memory
+    if (w == 0 && lg == 0 && lane == 0) {
+#pragma unroll 1
+      for (int k = 0; k < 8; ++k)
+        tma_store_2d(&tm_out, smem_u32(ostage + k * kOBoxBytes), 256 * (int)cta + 32 * k, (int32_t)row0);
+      bulk_commit();
+      bulk_wait_read0();
+    }
+  } else {
+    // no product (an empty range, a skipped or an aborted unit): zeros, by
+    // plain stores (copies of an aborted unit may still be landing in the ring)
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    g[lane] = have ? sp[lane] : z;
-    g[32 + lane] = have ? sp[32 + lane] : z;
+    for (int hr = 16 * (4 * w + lg); hr < min(16 * (4 * w + lg) + 16, p.Hq); ++hr) {
+      float4* g = reinterpret_cast<float4*>(p.dst_o + (row0 + hr) * kDv + 256 * cta);
+      g[lane] = z;
+      g[32 + lane] = z;
+    }
   }
   if (cta == 0 && w == 0 && h < p.Hq)
     p.dst_lse[row0 + h] = (have && l_tot > 0.f) ? (r_fin + log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
@@ -623,6 +634,7 @@ template <bool kLpt, bool kSmallBlocks>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
                 const __grid_constant__ CUtensorMap tm_qlat, const __grid_constant__ CUtensorMap tm_qrope,
+                const __grid_constant__ CUtensorMap tm_out,
                 const MlaParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -927,7 +939,7 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
     }
   } else if (warp < 12) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(kSoftRegs));
-    softmax_wg(p, sm, u, stages, scbuf, pmbuf, mxbuf, tmem, cta, warp, lane);
+    softmax_wg(p, tm_out, sm, u, stages, scbuf, pmbuf, mxbuf, tmem, cta, warp, lane);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kSendRegs));
     score_sender(p, sm, u, scbuf, tmem, cta, warp, lane);
@@ -1003,8 +1015,21 @@ cudaError_t launch_attn_mla_tc(const AttnArgs& a, const SplitPlan& plan) {
     p.dst_o = a.partial_out;
     p.dst_lse = a.lse;
   }
+  // the fp32 output rows [units x Hq][512], stored in 32-dim x Hq-row boxes
+  // (row coordinates are 32-bit)
+  const long long units = (long long)a.N * a.B * a.Lq * plan.n_split;
+  if (units == 0) return cudaSuccess;
+  if (units * a.Hq >= (1LL << 31)) return cudaErrorInvalidValue;
+  CUtensorMap tm_out;
+  const uint64_t odims[2] = {(uint64_t)kDv, (uint64_t)a.N * a.B * a.Lq * plan.n_split * a.Hq};
+  const uint64_t ostrides[1] = {(uint64_t)kDv * 4};
+  const uint32_t obox[2] = {32, (uint32_t)a.Hq};
+  if (!make_tensor_map(&tm_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.dst_o, 2, odims, ostrides, obox,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   const bool lpt = a.B <= kLptMaxBatch, small = a.bs < kNt;
-  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const MlaParams) =
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+               const MlaParams) =
       lpt ? (small ? mla_attn_kernel<true, true> : mla_attn_kernel<true, false>)
           : (small ? mla_attn_kernel<false, true> : mla_attn_kernel<false, false>);
   // the register split assumes the compiled launch count; refuse to launch
@@ -1015,10 +1040,8 @@ cudaError_t launch_attn_mla_tc(const AttnArgs& a, const SplitPlan& plan) {
   if (fa.numRegs * (int)kThreads < kSplitRegs) return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long units = (long long)a.N * a.B * a.Lq * plan.n_split;
-  if (units == 0) return cudaSuccess;
   if (units > (1LL << 30)) return cudaErrorInvalidValue;   // two CTAs a unit; 32-bit unit indices
-  kern<<<(unsigned)(2 * units), kThreads, kSmemBytes, a.stream>>>(tm_lat, tm_rope, tm_qlat, tm_qrope, p);
+  kern<<<(unsigned)(2 * units), kThreads, kSmemBytes, a.stream>>>(tm_lat, tm_rope, tm_qlat, tm_qrope, tm_out, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || plan.n_split <= 1) return e;
   return launch_split_combine(a, plan);

@@ -23,12 +23,12 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// bf16 tensor of `rank` dims (dims[0] innermost, in elements; strides[k] in
-// bytes for dims 1..rank-1), box `box` (elements), given swizzle.
+// Tensor of `rank` dims (dims[0] innermost, in elements; strides[k] in bytes
+// for dims 1..rank-1), box `box` (elements), given element type and swizzle.
 // Returns false when the map cannot be encoded (alignment, extents).
-inline bool make_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                                 const uint64_t* strides_bytes, const uint32_t* box,
-                                 CUtensorMapSwizzle swizzle) {
+inline bool make_tensor_map(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, int rank,
+                            const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                            CUtensorMapSwizzle swizzle) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t gdim[5];
@@ -41,10 +41,16 @@ inline bool make_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, con
     estride[i] = 1;
     if (i > 0) gstride[i - 1] = strides_bytes[i - 1];
   }
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
+  CUresult r = enc(m, dtype, (cuuint32_t)rank, const_cast<void*>(base),
                    gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+inline bool make_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                                 const uint64_t* strides_bytes, const uint32_t* box,
+                                 CUtensorMapSwizzle swizzle) {
+  return make_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides_bytes, box, swizzle);
 }
 
 }  // namespace dcp
