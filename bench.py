@@ -424,7 +424,7 @@ def run_ours(args):
     ws_bytes = dcp.dcp_decode_attn_workspace_size(desc, N)
     ws = torch.empty((max(ws_bytes, 1),), dtype=torch.uint8, device=dev) if ws_bytes else None
     attn, merge = step_fn(inst, po, lse, out, out_lse, ws)
-    launches_per_step = (2 if ws_bytes else 1) + 1
+    launches_per_step = dcp.dcp_decode_attn_launches(desc, N) + 1          # + the merge
     alg = algorithmic(w, inst.seq_lens.cpu().numpy())
 
     for _ in range(args.warmup):

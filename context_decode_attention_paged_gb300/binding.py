@@ -55,6 +55,8 @@ _lib.dcp_merge.restype = _i32
 _lib.dcp_merge.argtypes = [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]
 _lib.dcp_decode_attn_kernel_kind.restype = _i32
 _lib.dcp_decode_attn_kernel_kind.argtypes = [ctypes.POINTER(DcpAttnDesc), _i32]
+_lib.dcp_decode_attn_launches.restype = _i32
+_lib.dcp_decode_attn_launches.argtypes = [ctypes.POINTER(DcpAttnDesc), _i32]
 _lib.dcp_get_last_device_status.restype = _i32
 _lib.dcp_get_last_device_status.argtypes = [_vp]
 _lib.dcp_status_string.restype = ctypes.c_char_p
@@ -120,6 +122,11 @@ def dcp_build_slot_map(seq_lens, block_size, interleave, dcp_size, max_seq=None,
 
 def dcp_decode_attn_workspace_size(desc: DcpAttnDesc, dcp_size: int) -> int:
     return int(_lib.dcp_decode_attn_workspace_size(ctypes.byref(desc), dcp_size))
+
+
+def dcp_decode_attn_launches(desc: DcpAttnDesc, dcp_size: int) -> int:
+    """Kernels one dcp_decode_attn call enqueues for this shape (0: invalid)."""
+    return int(_lib.dcp_decode_attn_launches(ctypes.byref(desc), dcp_size))
 
 
 def dcp_decode_attn_kernel_kind(desc: DcpAttnDesc, dcp_size: int) -> int:

@@ -98,7 +98,8 @@ constexpr uint32_t kThreads = 512;                          // 4 warpgroups
 constexpr int kLaunchRegs = 128, kCtrlRegs = 48, kSendRegs = 96, kSoftRegs = 176;
 constexpr int kSplitRegs = 128 * kCtrlRegs + 256 * kSoftRegs + 128 * kSendRegs;   // 63,488
 static_assert(kSplitRegs <= 512 * kLaunchRegs, "register split exceeds the launch");
-constexpr int kLptMaxBatch = 128;
+constexpr int kLptMaxBatch = 128;        // up to this batch every CTA ranks the requests itself
+constexpr int kLptOrderMaxBatch = 16384; // up to this batch a pre-pass writes the order
 // TMEM columns (512 allocated)
 constexpr uint32_t kColQ = 0;      // 96 cols: 128 rows x latent dims 64-255 of the slice, bf16
 constexpr uint32_t kColS = 96;     // 2 x 64 cols fp32: partial scores of tile t in buffer t & 1
@@ -114,6 +115,7 @@ struct MlaParams {
   const __nv_bfloat16* q;
   const int32_t* block_tables;
   const int32_t* seq_lens;
+  const int32_t* order;   // longest-first request order from the pre-pass (null: rank in the kernel)
   float* dst_o;        // partial_out, or the split workspace
   float* dst_lse;
   int* status;
@@ -648,18 +650,18 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t cta = cluster_ctarank();          // 0 or 1
-  // kLpt (batches up to kLptMaxBatch): units in longest-request-first order.
-  // The block scheduler starts clusters in index order, so short units fill
-  // the tail.  Rank k of the order (length descending, index ascending) is
-  // found by counting; both CTAs of the pair compute the same request.  (The
-  // loaded request index costs registers, so large batches keep the plain
-  // order, whose indices are recomputed from the block index.)
+  // kLpt: units in longest-request-first order (length descending, index
+  // ascending).  The block scheduler starts clusters in index order, so short
+  // units fill the tail.  Batches up to kLptMaxBatch find rank k by counting
+  // in the kernel; larger ones read it from the pre-pass's order.  Both CTAs
+  // of the pair take the same request.
   const long long unit = blockIdx.x >> 1;
   int b_lpt = 0;
   if (kLpt) {
     const long long per_req = (long long)p.N * p.Lq * p.n_split;
     const int k_req = (int)(unit / per_req);
-    for (int j = tid; j < p.B; j += kThreads) {
+    if (p.order != nullptr && tid == 0) sm.req = p.order[k_req];
+    for (int j = tid; p.order == nullptr && j < p.B; j += kThreads) {
       const int sj = p.seq_lens[j];
       int rank = 0;
 #pragma unroll 1
@@ -955,6 +957,26 @@ mla_attn_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constan
   }
 }
 
+// Longest-first order of the requests: order[rank] = j, rank = number of
+// requests longer than j, or as long with a smaller index (each rank once).
+__global__ void __launch_bounds__(256) lpt_order_kernel(const int32_t* seq_lens, int B, int32_t* order) {
+  __shared__ int tile[256];
+  const int j = blockIdx.x * 256 + threadIdx.x;
+  const int sj = j < B ? seq_lens[j] : 0;
+  int rank = 0;
+  for (int base = 0; base < B; base += 256) {
+    __syncthreads();
+    if (base + threadIdx.x < B) tile[threadIdx.x] = seq_lens[base + threadIdx.x];
+    __syncthreads();
+    const int n = min(256, B - base);
+    for (int k = 0; k < n; ++k) {
+      const int si = tile[k];
+      rank += (si > sj) || (si == sj && base + k < j);
+    }
+  }
+  if (j < B) order[rank] = j;
+}
+
 }  // namespace
 
 bool mla_tc_supported(const AttnArgs& a) {
@@ -967,7 +989,13 @@ bool mla_tc_supported(const AttnArgs& a) {
 }
 
 SplitPlan plan_attn_mla_tc(const AttnArgs& a, int sm_count) {
-  return plan_splits(a, sm_count, kNt, 2 * a.Lq);
+  SplitPlan pl = plan_splits(a, sm_count, kNt, 2 * a.Lq);
+  if (a.B > kLptMaxBatch && a.B <= kLptOrderMaxBatch) {
+    pl.lpt_order = true;
+    pl.order_offset = (pl.ws_bytes + 255) & ~size_t(255);
+    pl.ws_bytes = pl.order_offset + (((size_t)a.B * 4 + 255) & ~size_t(255));
+  }
+  return pl;
 }
 
 cudaError_t launch_attn_mla_tc(const AttnArgs& a, const SplitPlan& plan) {
@@ -1027,7 +1055,16 @@ cudaError_t launch_attn_mla_tc(const AttnArgs& a, const SplitPlan& plan) {
   if (!make_tensor_map(&tm_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.dst_o, 2, odims, ostrides, obox,
                        CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  const bool lpt = a.B <= kLptMaxBatch, small = a.bs < kNt;
+  const bool lpt = a.B <= kLptOrderMaxBatch, small = a.bs < kNt;
+  p.order = nullptr;
+  if (plan.lpt_order) {
+    if (a.workspace == nullptr || a.workspace_bytes < plan.ws_bytes) return cudaErrorInvalidValue;
+    int32_t* order = reinterpret_cast<int32_t*>(static_cast<char*>(a.workspace) + plan.order_offset);
+    lpt_order_kernel<<<(unsigned)((a.B + 255) / 256), 256, 0, a.stream>>>(a.seq_lens, a.B, order);
+    cudaError_t eo = cudaGetLastError();
+    if (eo != cudaSuccess) return eo;
+    p.order = order;
+  }
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                const MlaParams) =
       lpt ? (small ? mla_attn_kernel<true, true> : mla_attn_kernel<true, false>)

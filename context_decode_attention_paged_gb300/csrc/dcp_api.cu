@@ -169,6 +169,8 @@ SplitPlan plan_splits(const AttnArgs& a, int sm_count, int tile_tokens, int unit
   if (per < tile_tokens) per = tile_tokens;
   n = (max_local + per - 1) / per;
   if (n < 1) n = 1;
+  p.lpt_order = false;
+  p.order_offset = 0;
   p.n_split = (int)n;
   p.split_tokens = (int)std::min<long long>(per, 1LL << 30);
   p.ws_bytes = 0;
@@ -323,6 +325,13 @@ dcp_status_t dcp_get_last_device_status(void* stream) {
   if (cudaMemsetAsync(p, 0, sizeof(int), s) != cudaSuccess) return DCP_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return DCP_ERR_CUDA;
   return static_cast<dcp_status_t>(v);
+}
+
+int32_t dcp_decode_attn_launches(const dcp_attn_desc_t* d, int32_t dcp_size) {
+  AttnArgs a{};
+  if (make_args(d, dcp_size, 1, 1.0f, d ? d->q_len : 1, &a) != DCP_OK) return 0;
+  const SplitPlan plan = plan_for(a, select_impl(a), device_sm_count());
+  return 1 + (plan.n_split > 1 ? 1 : 0) + (plan.lpt_order ? 1 : 0);
 }
 
 int32_t dcp_decode_attn_kernel_kind(const dcp_attn_desc_t* d, int32_t dcp_size) {

@@ -31,12 +31,15 @@ struct AttnArgs {
 struct SplitPlan {
   int n_split;           // KV splits per (shard, request[, query]) unit
   int split_tokens;      // local tokens per split (multiple of the kernel tile)
-  size_t ws_bytes;       // workspace for split partials (0 when n_split == 1)
+  size_t ws_bytes;       // workspace bytes (split partials, request order)
+  bool lpt_order;        // a pre-pass writes the longest-first request order
+  size_t order_offset;   // where it goes in the workspace (int32 [B])
 };
 
 // Workspace layout when n_split > 1:
 //   ws_o   fp32 [N][B][Lq][n_split][Hq][Dv]
 //   ws_lse fp32 [N][B][Lq][n_split][Hq]       (after ws_o, 256-byte aligned)
+// then, 256-byte aligned, the request order when lpt_order is set.
 SplitPlan plan_splits(const AttnArgs& a, int sm_count, int tile_tokens, int units_per_split);
 
 int device_sm_count();

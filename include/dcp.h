@@ -260,6 +260,12 @@ DCP_API dcp_status_t dcp_kv_cache_write(const dcp_attn_desc_t* d, const void* ne
  * caller see in advance that a shape falls back to the CUDA-core kernel. */
 DCP_API int32_t dcp_decode_attn_kernel_kind(const dcp_attn_desc_t* d, int32_t dcp_size);
 
+/* How many kernels one dcp_decode_attn call enqueues for this shape: the
+ * attention kernel, plus the combine of KV splits when a shard is split, plus
+ * the request-order pre-pass of the MLA tensor-core kernel for batches of
+ * 129 to 16384 requests.  0 for an invalid descriptor.  Host only. */
+DCP_API int32_t dcp_decode_attn_launches(const dcp_attn_desc_t* d, int32_t dcp_size);
+
 /* Reads `stream`'s status word (the first device-side error of the calls
  * enqueued on that stream since the last read; DCP_OK if none) and clears it.
  * The read and the clear are enqueued on `stream` and the call then waits for

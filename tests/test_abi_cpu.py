@@ -213,3 +213,26 @@ def test_kernel_kind_reports_the_kernel_a_shape_runs(lib, shape, N, want):
     sees a fall-back to the CUDA-core kernel before launching."""
     desc = lib.make_desc(*shape)
     assert lib.dcp_decode_attn_kernel_kind(desc, N) == getattr(lib, "DCP_KERNEL_" + want)
+
+
+@pytest.mark.parametrize("shape,N,want_launches,want_ws", [
+    # MLA batch 512: the longest-first request order comes from a pre-pass
+    # into the workspace (int32 per request)
+    (("mla", 512, 1, 128, 1, 576, 512, 128, 512 * 8 * 80, 80), 8, 2, 2048),
+    # MLA batch 32 ranks its requests in the kernel: nothing extra
+    (("mla", 32, 1, 128, 1, 576, 512, 128, 32 * 8 * 80, 80), 8, 1, 0),
+    # a small batch with long shards also splits them: attention + combine
+    (("mla", 1, 4, 128, 1, 576, 512, 128, 8 * 196, 196), 8, 2, None),
+    (("gqa", 64, 1, 64, 4, 128, 128, 128, 64 * 4 * 60, 60), 4, 1, 0),
+])
+def test_launch_count_and_workspace(lib, shape, N, want_launches, want_ws):
+    """The kernels a call enqueues, as the benchmark counts them, and the
+    workspace the MLA request order takes."""
+    desc = lib.make_desc(*shape)
+    assert lib.dcp_decode_attn_launches(desc, N) == want_launches
+    ws = lib.raw_lib().dcp_decode_attn_workspace_size(ctypes.byref(desc), N)
+    if want_ws is not None:
+        assert ws == want_ws
+    else:
+        assert ws > 0
+    assert lib.dcp_decode_attn_launches(lib.make_desc("mla", 4, 1, 128, 2, 576, 512, 128, 100, 10), N) == 0
