@@ -7,17 +7,21 @@
 // section "Multi-head Latent Attention (MLA) 後端" (one low-rank latent KV head
 // shared by every query head).
 //
-// Work unit = (shard r, request b, query i, KV split s), longest request first
-// for batches up to 128, run by a cluster of two CTAs.  With 128 query heads
-// the fp32 output (128 x 512) fills a whole SM's tensor memory and the bf16
-// query (128 x 576) does not fit next to a KV ring in shared memory, so the
-// pair splits the head dimensions for the two products:
+// Work unit = (shard r, request b, query i, KV split s), run by a cluster of
+// two CTAs, longest request first (up to 128 requests every CTA ranks them
+// itself; larger batches read the order from a pre-pass kernel).  With 128
+// query heads the fp32 output (128 x 512) fills a whole SM's tensor memory and
+// the bf16 query (128 x 576) does not fit next to a KV ring in shared memory,
+// so the pair splits the head dimensions for the two products:
 //   CTA c holds query dims D_c = latent[256c, +256) + rope[32c, +32) (latent
-//   dims 64-255 of the slice in TMEM, the rest in shared memory), streams the same dims of each 64-token KV tile (TMA,
-//   128B/64B swizzle), computes the partial scores S_c = Q_c K_c^T (M = 128
-//   heads, N = 64 tokens, K = 288; A from TMEM and shared memory) and
-//   accumulates O_c += P V_c for output dims [256c, +256) (M = 128, N = 256,
-//   K = 64; P from TMEM, V read MN-major out of the latent part of its tile),
+//   dims 64-255 of the slice in TMEM, the rest in shared memory, all staged by
+//   TMA), streams the same dims of each 64-token KV tile (TMA, 128B/64B
+//   swizzle; one box per tile, or one per block for blocks of 8-32 tokens),
+//   computes the partial scores S_c = Q_c K_c^T (M = 128 heads, N = 64
+//   tokens, K = 288; A from TMEM and shared memory) into one of two score
+//   buffers, and accumulates O_c += P V_c for output dims [256c, +256)
+//   (M = 128, N = 256, K = 64; P from TMEM, V read MN-major out of the latent
+//   part of its tile),
 // and splits the tokens for the softmax: CTA c owns tokens [32c, +32) of
 // every tile.  It sends the peer its partial scores of the peer's 32 tokens
 // (16-bit block floating point, one power-of-two scale per head and tile, and a
@@ -28,6 +32,8 @@
 // the same reference to the tile; the bf16 probabilities of its 32 tokens then
 // go to the peer with their row sum, and each CTA writes both halves into its
 // P buffer in TMEM.  Every KV byte is loaded once and no MMA is repeated.
+// With fewer than 128 query heads (16 or more) the MMA rows past Hq hold the
+// next query rows of the tensor: computed, never written.
 //
 // Reference.  P = exp2(score * scale * log2(e) - R) in the log2 domain; R(t)
 // is the running maximum, updated lazily: it moves to the tile's maximum only
@@ -38,18 +44,17 @@
 // Warp roles (512 threads; setmaxnreg moves registers to the softmax warps):
 //   warp 0      TMA producer (5-stage ring of 36 KB tiles)
 //   warp 1      PV MMA issuer, TMEM owner; PV(t) goes out once the score MMAs
-//               of tile t+2 are issued, so that each tile's score MMAs run back
-//               to back (the single score buffer waits on them) and PV fills
-//               the gap while the scores are read out
+//               of tile t+1 are issued, so that each tile's score MMAs run
+//               back to back and PV fills the gap while the scores are read
 //   warp 2      score (QK^T) MMA issuer
 //   warps 4-7   softmax warpgroup 0: tiles 0, 2, 4, ...
 //   warps 8-11  softmax warpgroup 1: tiles 1, 3, 5, ...  The two warpgroups
 //               overlap on consecutive tiles: while one waits for the peer's
 //               half of its tile, the other computes the next; R(t) passes
-//               from one to the other through shared memory
+//               from one to the other through shared memory.  At the end
+//               they stage O in the idle ring, from where TMA stores it
 //   warps 12-15 score senders: read the peer's half of every tile's partial
-//               scores out of TMEM and push them to the peer; they also stage
-//               the query's rope dims in shared memory
+//               scores out of TMEM and push them to the peer
 // Every wait is bounded; on expiry the kernel records DCP_ERR_TIMEOUT, drains
 // its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
