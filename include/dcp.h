@@ -127,8 +127,12 @@ DCP_API dcp_status_t dcp_build_slot_map(const int32_t* seq_lens, int32_t batch, 
                                 void* stream);
 
 /* Bytes of device scratch dcp_decode_attn needs for this shape (0 is
- * possible).  Depends on the shape only (not on the contents of seq_lens).
- * Returns 0 and sets nothing for an invalid descriptor. */
+ * possible): the partial outputs of KV splits when a shard's keys are split
+ * across several work units (small batches, long contexts), and for MLA
+ * batches of 129 to 16384 requests the longest-first request order (4 bytes a
+ * request) that a pre-pass writes.  Depends on the shape only (not on the
+ * contents of seq_lens).  Returns 0 and sets nothing for an invalid
+ * descriptor. */
 DCP_API size_t dcp_decode_attn_workspace_size(const dcp_attn_desc_t* d, int32_t dcp_size);
 
 /* Steps a2-a5: per-shard partial attention with LSE.
