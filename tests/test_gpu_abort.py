@@ -38,12 +38,17 @@ def hooks():
     lib.dcp_testing_set_hooks(0, -1)
 
 
-# one work unit each: MLA with one shard and one request (one cluster pair),
-# GQA with one shard, one request and one KV head (one CTA)
+# MLA with one shard and one request (one cluster pair), GQA with one shard,
+# one request and one KV head (one CTA); then two MLA paths of their own
 CASES = [
     ("mla_32", dict(batch=1, lengths=("fixed", 300), dcp_size=1)),
     ("mla_32", dict(batch=1, lengths=("fixed", 100), dcp_size=1)),
     ("qwen_gqa", dict(batch=1, num_q_heads=16, num_kv_heads=1, lengths=("fixed", 700), dcp_size=1)),
+    # the MLA instance for small blocks (four TMA boxes a tile)
+    ("mla_32", dict(batch=1, block_size=16, lengths=("fixed", 300), dcp_size=1, interleave=16)),
+    # an MLA batch above 128: units in the order a pre-pass writes (every unit
+    # times out; they run in two waves of clusters)
+    ("mla_32", dict(batch=130, lengths=("uniform", 100, 200), dcp_size=1)),
 ]
 
 
