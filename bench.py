@@ -82,9 +82,9 @@ def algorithmic(w: wl.Workload, seq_lens) -> dict:
 # source the counters were taken on: once the source changes, traffic is
 # reported as null.
 NCU_TRAFFIC_RATIO = {
-    "mla": ("ed1f3f02c90ad3fb", 1.00618, "attn_mla_tc.cu"),
+    "mla": ("08235e44124c0ac7", 1.00528, "attn_mla_tc.cu"),
     "gqa": ("f6e04d4ccaedbfff", 1.00386, "attn_gqa_tc.cu"),
-    "mla_chunk64": ("ed1f3f02c90ad3fb", 1.05268, "attn_mla_tc.cu"),
+    "mla_chunk64": ("08235e44124c0ac7", 1.03412, "attn_mla_tc.cu"),
 }
 
 
