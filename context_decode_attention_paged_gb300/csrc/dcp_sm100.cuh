@@ -43,11 +43,6 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
   return out;
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};"
-               :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
-}
-
 // Asynchronous 16-byte store into another CTA's shared memory; on arrival it
 // counts 16 bytes of transaction on that CTA's mbarrier `cluster_bar` (both
 // addresses from mapa).  The sender needs no fence.
@@ -55,12 +50,6 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
                                             uint32_t cluster_bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
                :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar) : "memory");
-}
-
-// 8-byte variant of st_async_v4.
-__device__ __forceinline__ void st_async_v2(uint32_t addr, float a, float b, uint32_t cluster_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
-               :: "r"(addr), "f"(a), "f"(b), "r"(cluster_bar) : "memory");
 }
 
 // 4-byte variant of st_async_v4.
