@@ -36,9 +36,15 @@ def _worker(rank, world, port, out_dir):
         bench.barrier(world)
         mx = bench.max_over_ranks(10.0 + rank * 5.0, world)     # rank times 10, 15
         sm = bench.sum_over_ranks(100.0 * (rank + 1), world)    # rank work 100, 200
+        # the job's rate: all ranks' work over the slowest rank's time
+        rate, slow = bench.whole_job_rate(100.0 * (rank + 1), 10.0 + rank * 5.0, world)
+        # every rank draws its own workload of the same shape
+        w = bench.rank_workload("mla_512", rank)
+        lens = bench.wl.make_seq_lens(w)
         bench.barrier(world)
         with open(os.path.join(out_dir, f"r{rank}.json"), "w") as f:
-            json.dump({"max": mx, "sum": sm}, f)
+            json.dump({"max": mx, "sum": sm, "rate": rate, "slow": slow, "seed": w.seed,
+                       "batch": w.batch, "lens_head": lens[:4].tolist()}, f)
     finally:
         td.destroy_process_group()
 
@@ -47,9 +53,13 @@ def test_rank_reductions_gloo(tmp_path):
     world = 2
     mp.start_processes(_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world,
                        join=True, start_method="spawn")
-    for r in range(world):
-        got = json.load(open(tmp_path / f"r{r}.json"))
-        assert got == {"max": 15.0, "sum": 300.0}
+    got = [json.load(open(tmp_path / f"r{r}.json")) for r in range(world)]
+    for g in got:
+        assert g["max"] == 15.0 and g["sum"] == 300.0
+        assert g["rate"] == 300.0 / 15e-3 and g["slow"] == 15.0
+    assert got[0]["batch"] == got[1]["batch"] == 512
+    assert got[0]["seed"] + 1 == got[1]["seed"]
+    assert got[0]["lens_head"] != got[1]["lens_head"]      # independent draws
 
 
 def test_single_rank_reductions_are_identity():
