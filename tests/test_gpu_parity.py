@@ -121,6 +121,13 @@ ATTN_CASES = [
     ("mla_32", dict(batch=2, num_q_heads=16, q_len=4, lengths=("uniform", 300, 1500), dcp_size=2,
                     interleave=1)),
     ("mla_32", dict(batch=3, num_q_heads=40, lengths=("uniform", 700, 3000), dcp_size=8)),
+    # combinations: a batch ordered by the pre-pass with 64 heads; 16-token
+    # blocks under causal MTP queries at interleave 1; 32 heads with KV splits
+    # (a long single request) and their combine
+    ("mla_32", dict(batch=130, num_q_heads=64, lengths=("uniform", 64, 400), dcp_size=2)),
+    ("mla_32", dict(batch=2, block_size=16, q_len=4, lengths=("uniform", 500, 2500), dcp_size=4,
+                    interleave=1)),
+    ("mla_mtp", dict(num_q_heads=32, lengths=("fixed", 40000), dcp_size=8)),
     # group sizes: 1 (one real row of a 16-row tile) and 8 with Lq 3 (24 rows of a 32-row tile)
     ("qwen_gqa", dict(batch=2, num_q_heads=8, num_kv_heads=8, lengths=("uniform", 300, 900), dcp_size=2)),
     ("qwen_gqa", dict(batch=2, num_q_heads=32, num_kv_heads=4, q_len=3, lengths=("uniform", 300, 900),
